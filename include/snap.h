@@ -1,0 +1,196 @@
+/*
+ * snap.h -- C ABI of libsnap: the SnapStream fixed-size KV cache on GB300 (sm_103a).
+ *
+ * Method: SnapStream: Efficient Long Sequence Decoding on Dataflow Accelerators
+ * (arXiv 2511.03092).  Its episode companion page, section "Fixed-Size Cache
+ * Layout", fixes one static cache per sequence built once at prefill,
+ *
+ *        [ L_sink sink tokens | K SnapKV-selected middle tokens | L_recent recent ]
+ *
+ * with the three sizes as configurable hyperparameters; section "Ring Buffer vs.
+ * Naive Slicing" fixes that decode only rotates the recent window, writing each
+ * new token into a fixed index (scatter, no gather, no concat).  The SnapKV
+ * step ("pooling-based top-K selection", section "Infinity-Bench KV Retrieval")
+ * scores every prefix position by the softmax of the last W prompt queries
+ * (the observation window), summed over the window and over the query heads
+ * that share a KV head, max-pools the scores with an odd kernel P, and keeps the
+ * K best middle positions (ties go to the lower position; kept in ascending
+ * order).
+ *
+ * Conventions (every entry point):
+ *  - All data pointers are DEVICE pointers unless a comment says host.  bf16 data
+ *    is passed as void*; it must be 16-byte aligned, as must every row stride in
+ *    bytes.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Every call is asynchronous on that stream, performs no host synchronisation
+ *    and allocates no memory: buffers and workspaces are owned by the caller.
+ *  - Argument and shape errors are detected on the host and returned synchronously;
+ *    nothing is launched then.  Errors found by a kernel (a slot index out of range,
+ *    a bounded wait that expired) are recorded in the cache's device status word and
+ *    read back by snap_check_device().
+ *  - Not thread-safe per cache handle: calls on one handle must be ordered by the
+ *    caller (same stream, or events).
+ */
+#ifndef SNAP_H
+#define SNAP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SNAP_OK = 0,
+    SNAP_ERR_INVALID_ARG = 1,  /* null pointer, misaligned pointer/stride, bad slot count */
+    SNAP_ERR_SHAPE = 2,        /* sizes violate the method's preconditions */
+    SNAP_ERR_UNSUPPORTED = 3,  /* valid for the method, not implemented by these kernels */
+    SNAP_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    SNAP_ERR_TIMEOUT = 5,      /* a kernel's bounded wait expired (device status word) */
+    SNAP_ERR_DEVICE_CHECK = 6  /* a kernel rejected an index (device status word) */
+} snap_status;
+
+/* Layout of the attention the cache serves. */
+enum { SNAP_LAYOUT_GQA = 0, SNAP_LAYOUT_MLA = 1 };
+
+/*
+ * Cache configuration.
+ *  layout      SNAP_LAYOUT_GQA: separate K and V, n_q_heads / n_kv_heads query heads per
+ *              KV head (query head i reads KV head i / G).  Supported: d_qk == d_v == 128,
+ *              G = n_q_heads / n_kv_heads <= 8.
+ *              SNAP_LAYOUT_MLA: one latent KV head (n_kv_heads == 1); the key row is
+ *              [latent (d_v) | rope (d_qk - d_v)] and the value is its first d_v columns
+ *              (absorbed-query attention, DeepSeek-V2 style).  Supported: d_qk == 576,
+ *              d_v == 512, n_q_heads a multiple of 16.
+ *  L_sink, K, L_recent   segment sizes; C = L_sink + K + L_recent slots per KV head.
+ *  W           observation window (last W prompt queries); 1 <= W <= L_recent.
+ *  P           max-pool kernel width, odd, >= 1.
+ *  sm_scale    softmax scale applied to q.k (> 0).
+ */
+typedef struct {
+    int layout;
+    int n_q_heads;
+    int n_kv_heads;
+    int d_qk;
+    int d_v;
+    int L_sink;
+    int K;
+    int L_recent;
+    int W;
+    int P;
+    float sm_scale;
+} snap_config;
+
+/* Per-sequence bookkeeping kept on the device (one entry per cache slot). */
+typedef struct {
+    int32_t S;       /* prompt length at compression */
+    int32_t T;       /* current length: S + appended tokens */
+    int32_t R0;      /* first prompt position that was written into the ring */
+    int32_t n_sink;  /* valid sink slots = min(L_sink, S) */
+    int32_t n_mid;   /* valid middle slots = min(K, R0 - n_sink) */
+    int32_t pad[3];
+} snap_seq_meta;
+
+/* Device addresses of the regions a cache occupies inside the caller's buffer. */
+typedef struct {
+    void* k;               /* bf16 [max_batch][n_kv_heads][C][d_qk] */
+    void* v;               /* bf16 [max_batch][n_kv_heads][C][d_v]; NULL for MLA */
+    snap_seq_meta* meta;   /* [max_batch] */
+    int32_t* sel;          /* [max_batch][n_kv_heads][K] selected middle positions */
+    int32_t* status;       /* device status word: [0] = snap_status, [1..3] = detail */
+    int64_t C;             /* slots per KV head */
+    int max_batch;
+} snap_cache_view;
+
+typedef struct snap_cache snap_cache; /* opaque host-side handle */
+
+/* Human-readable text of a status code (static string, never NULL). */
+const char* snap_status_string(int status);
+
+/* Library ABI version (incremented on incompatible changes). */
+int snap_abi_version(void);
+
+/* Checks a configuration against the method's preconditions and these kernels. */
+snap_status snap_config_check(const snap_config* cfg);
+
+/*
+ * Bytes of device memory a cache of `max_batch` sequences needs (host call, no
+ * CUDA).  The cache is exactly C / T_full of a full KV cache of T_full tokens:
+ * for C = 32768 against 131072 tokens that is 4x smaller (the page's "4.0x lower
+ * KV memory").
+ */
+snap_status snap_cache_bytes(const snap_config* cfg, int max_batch, size_t* bytes);
+
+/*
+ * Binds a cache to a caller-owned device buffer of at least snap_cache_bytes()
+ * bytes (256-byte aligned).  The handle owns host state only; the buffer stays the
+ * caller's and must outlive the handle.  Zeroes the whole buffer on `stream`
+ * (every slot starts empty).  *out receives the handle.
+ */
+snap_status snap_cache_create(const snap_config* cfg, int max_batch, void* dev_buf,
+                              size_t bytes, void* stream, snap_cache** out);
+void snap_cache_destroy(snap_cache* cache);
+
+/* Fills *out with the device addresses of the cache regions (host call). */
+snap_status snap_cache_view_get(const snap_cache* cache, snap_cache_view* out);
+
+/* Workspace bytes snap_compress() needs for prompts of up to S_max tokens. */
+snap_status snap_compress_ws_bytes(const snap_config* cfg, int64_t S_max, size_t* bytes);
+
+/*
+ * Prefill compression of one sequence into cache slot `slot` (0 <= slot < max_batch),
+ * the SnapKV + StreamingLLM fusion of the "Fixed-Size Cache Layout" section.
+ *  K       bf16 keys: element (token j, kv head h, e) at K + j*tok_stride + h*head_stride + e
+ *          (strides in elements; post-RoPE keys; MLA: the [latent | rope] rows).
+ *  V       bf16 values with the same strides (GQA); must be NULL for MLA.
+ *  S       prompt length >= 1.  Scoring runs only when the middle [L_sink, S - L_recent)
+ *          holds more than K positions.
+ *  Q_obs   bf16 [W][n_q_heads][d_qk], the queries of prompt positions S-W .. S-1.
+ *  ws      device workspace of at least snap_compress_ws_bytes(cfg, S) bytes.
+ * Writes every slot of the sequence (unused ones zeroed), the selected positions and
+ * the meta {S, T = S, R0, n_sink, n_mid}.  The softmax denominator of each window row
+ * runs over all keys up to the query's own position (the prefill attention's row).
+ */
+snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
+                          int64_t tok_stride, int64_t head_stride, const void* Q_obs,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Decode-step append for a continuous batch ("Ring Buffer vs. Naive Slicing"): for each
+ * b < n, the new token of sequence slots[b] (position T) is written into ring slot
+ * L_sink + K + (T mod L_recent), then T += 1.  No gather, no concat.
+ *  slots   device int32 [n], distinct cache slots (a repeated slot is a caller error)
+ *  k_new   bf16 [n][n_kv_heads][d_qk];  v_new bf16 [n][n_kv_heads][d_v] (NULL for MLA)
+ */
+snap_status snap_decode_append(snap_cache* cache, const int32_t* slots, int n, const void* k_new,
+                               const void* v_new, void* stream);
+
+/* Workspace bytes snap_decode_attn() needs for batches of up to max_n sequences. */
+snap_status snap_decode_attn_ws_bytes(const snap_config* cfg, int max_n, size_t* bytes);
+
+/*
+ * Split-KV decode attention over the fixed-size cache for a continuous batch whose
+ * sequences sit at different ring offsets.  For each b < n and query head i, a plain
+ * softmax over the VALID slots of sequence slots[b] (sinks < n_sink, middle < n_mid,
+ * ring slots holding positions max(R0, T - L_recent) .. T-1) of sm_scale * q.k,
+ * weighted sum of the values.  The query attends to what the cache holds now: call
+ * snap_decode_append() first to include the current token.
+ *  q     bf16 [n][n_q_heads][d_qk];  out bf16 [n][n_q_heads][d_v]
+ *  ws    device workspace of snap_decode_attn_ws_bytes(cfg, n) bytes
+ * A full (uncompressed) KV cache is the same call on a cache configured with
+ * L_sink = 0, K = 0, L_recent = maximum length.
+ */
+snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, const void* q,
+                             void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, reads the device status word, clears it, and returns it
+ * (SNAP_OK when no kernel reported an error since the last check).
+ */
+snap_status snap_check_device(snap_cache* cache, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SNAP_H */
