@@ -1,0 +1,535 @@
+// k_decode.cu -- split-KV decode attention over the fixed-size cache.
+//
+// SnapStream episode companion page, "Prefill / Decode Pipeline": decode is
+// memory-bound, so the cache bytes streamed per step set the time per token.
+// Each CTA streams one contiguous range of cache slots of one (sequence, KV head)
+// once from HBM and produces an un-normalised partial (max, sum, O) per query
+// head; a merge kernel combines the splits (flash-decoding's log-sum-exp merge).
+// Invalid slots (unused middle slots, ring slots not holding a live position)
+// are masked; whole tiles with no valid slot are not read.
+#include "kernels.cuh"
+
+namespace snap {
+
+namespace {
+
+constexpr float NEG_INF = -__builtin_huge_valf();
+
+// ===================================================================== GQA
+// d = 128, G <= 8 query heads per KV head.  Keys sit on the MMA's M side
+// (16 keys per m16 tile), the G heads on the N side (n8): S^T = K Q^T, then
+// O^T += V^T P^T with P^T moved into B-fragment layout by movmatrix.
+constexpr int GD = 128;
+constexpr int G_ROWB = GD * 2;                              // 256 bytes per key row
+constexpr int G_WARPS = 4;
+constexpr int G_STAGES = 3;
+constexpr int G_STAGE_BYTES = GQA_KEYS * G_ROWB * 2;        // K + V tile = 16 KB
+constexpr int G_SMEM = G_WARPS * G_STAGES * G_STAGE_BYTES;  // 192 KB
+
+__global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const DevConfig& c = a.cfg;
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = a.slots[b];
+    if (slot < 0 || slot >= c.max_batch) {
+        if (threadIdx.x == 0 && split == 0 && h == 0)
+            report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
+        if (a.splits == 1)  // otherwise the merge kernel writes the zeros
+            for (int i = threadIdx.x; i < c.G * GD; i += blockDim.x)
+                a.out[((size_t)b * c.Hq + (size_t)h * c.G) * GD + i] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const snap_seq_meta m = a.meta[slot];
+    SlotValidity sv;
+    sv.init(m, c);
+    const size_t row0 = ((size_t)slot * c.Hkv + h) * (size_t)c.C;
+    const bf16* kbase = a.kc + row0 * GD;
+    const bf16* vbase = a.vc + row0 * GD;
+
+    // Q^T as B fragments: n = head (lane/4), k = d.
+    uint32_t qf[8][2];
+    {
+        const int hq = lane >> 2;
+        const bf16* qp = a.q + ((size_t)b * c.Hq + (size_t)h * c.G + (hq < c.G ? hq : 0)) * GD;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+            if (hq < c.G) {
+                qf[ks][0] = *reinterpret_cast<const uint32_t*>(qp + ks * 16 + 2 * (lane & 3));
+                qf[ks][1] = *reinterpret_cast<const uint32_t*>(qp + ks * 16 + 8 + 2 * (lane & 3));
+            } else {
+                qf[ks][0] = qf[ks][1] = 0u;
+            }
+        }
+    }
+
+    const int ntiles = (c.C + GQA_KEYS - 1) / GQA_KEYS;
+    const int t_begin = split * a.tiles_per_split;
+    const int t_end = min(ntiles, t_begin + a.tiles_per_split);
+    const uint32_t wsm = smem_u32(smem) + warp * G_STAGES * G_STAGE_BYTES;
+
+    auto next_tile = [&](int t) {
+        while (t < t_end && !sv.any_valid(t * GQA_KEYS, min(c.C, (t + 1) * GQA_KEYS))) t += G_WARPS;
+        return t;
+    };
+    auto load_tile = [&](int t, int st) {
+        const uint32_t sk = wsm + st * G_STAGE_BYTES;
+        const uint32_t svv = sk + GQA_KEYS * G_ROWB;
+#pragma unroll 4
+        for (int i = lane; i < GQA_KEYS * 16; i += 32) {
+            const int r = i >> 4, ch = i & 15;
+            const int key = t * GQA_KEYS + r;
+            const bool ok = key < c.C;
+            const size_t off = (size_t)(ok ? key : 0) * GD + ch * 8;
+            cp_async16(sk + swz(r, ch, G_ROWB), kbase + off, ok ? 16 : 0);
+            cp_async16(svv + swz(r, ch, G_ROWB), vbase + off, ok ? 16 : 0);
+        }
+    };
+
+    float m_run[2] = {NEG_INF, NEG_INF};
+    float l_run[2] = {0.f, 0.f};
+    float o[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    int t_load = next_tile(t_begin + warp);
+    int t_comp = t_load;
+#pragma unroll
+    for (int st = 0; st < G_STAGES - 1; ++st) {
+        if (t_load < t_end) {
+            load_tile(t_load, st);
+            t_load = next_tile(t_load + G_WARPS);
+        }
+        cp_async_commit();
+    }
+    int st_comp = 0, st_load = G_STAGES - 1;
+    const float sl2 = c.scale_log2;
+    while (t_comp < t_end) {
+        if (t_load < t_end) {
+            load_tile(t_load, st_load);
+            t_load = next_tile(t_load + G_WARPS);
+        }
+        cp_async_commit();
+        cp_async_wait<G_STAGES - 1>();
+        __syncwarp();
+
+        const uint32_t sk = wsm + st_comp * G_STAGE_BYTES;
+        const uint32_t svv = sk + GQA_KEYS * G_ROWB;
+        float s[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const int r = mt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                const int ch = ks * 2 + (lane >> 4);
+                uint32_t af[4];
+                ldsm_x4(sk + swz(r, ch, G_ROWB), af[0], af[1], af[2], af[3]);
+                mma_bf16(s[mt], af, qf[ks][0], qf[ks][1]);
+            }
+        }
+        // mask + scale into the base-2 domain; per-head tile max
+        float mx0 = NEG_INF, mx1 = NEG_INF;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int key = t_comp * GQA_KEYS + mt * 16 + (lane >> 2) + 8 * half;
+                const bool ok = key < c.C && sv.valid(key);
+                s[mt][2 * half + 0] = ok ? s[mt][2 * half + 0] * sl2 : NEG_INF;
+                s[mt][2 * half + 1] = ok ? s[mt][2 * half + 1] * sl2 : NEG_INF;
+                mx0 = fmaxf(mx0, s[mt][2 * half + 0]);
+                mx1 = fmaxf(mx1, s[mt][2 * half + 1]);
+            }
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+        }
+        const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+        const float al0 = mn0 == NEG_INF ? 1.f : ex2(m_run[0] - mn0);
+        const float al1 = mn1 == NEG_INF ? 1.f : ex2(m_run[1] - mn1);
+        m_run[0] = mn0;
+        m_run[1] = mn1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                // weights rounded to bf16 here, so that the normaliser sums exactly
+                // the weights the P V product uses
+                float p0 = mn0 == NEG_INF ? 0.f : bf16_round(ex2(s[mt][2 * half + 0] - mn0));
+                float p1 = mn1 == NEG_INF ? 0.f : bf16_round(ex2(s[mt][2 * half + 1] - mn1));
+                s[mt][2 * half + 0] = p0;
+                s[mt][2 * half + 1] = p1;
+                ps0 += p0;
+                ps1 += p1;
+            }
+        l_run[0] = l_run[0] * al0 + ps0;
+        l_run[1] = l_run[1] * al1 + ps1;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt) {
+            o[dt][0] *= al0;
+            o[dt][1] *= al1;
+            o[dt][2] *= al0;
+            o[dt][3] *= al1;
+        }
+        // O^T[d][head] += V^T[d][key] * P^T[key][head]
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const uint32_t b0 = movmatrix_t(pack_bf16(s[mt][0], s[mt][1]));
+            const uint32_t b1 = movmatrix_t(pack_bf16(s[mt][2], s[mt][3]));
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt) {
+                const int r = mt * 16 + (lane & 7) + ((lane >> 4) << 3);
+                const int ch = dt * 2 + ((lane >> 3) & 1);
+                uint32_t af[4];
+                ldsm_x4_t(svv + swz(r, ch, G_ROWB), af[0], af[1], af[2], af[3]);
+                mma_bf16(o[dt], af, b0, b1);
+            }
+        }
+        __syncwarp();
+        t_comp = next_tile(t_comp + G_WARPS);
+        st_comp = (st_comp + 1) % G_STAGES;
+        st_load = (st_load + 1) % G_STAGES;
+    }
+    cp_async_wait<0>();
+
+    // per-head sums over the lanes holding the same head columns
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], x);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], x);
+    }
+    __syncthreads();
+    // cross-warp merge through shared memory (pipeline buffers are free now)
+    float* ob = reinterpret_cast<float*>(smem);                 // [warps][8 heads][128]
+    float* mlb = ob + G_WARPS * 8 * GD;                         // [warps][8][2]
+    {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int d = dt * 16 + g + 8 * (i >> 1);
+                const int hh = 2 * t + (i & 1);
+                ob[(warp * 8 + hh) * GD + d] = o[dt][i];
+            }
+        if (lane < 4) {
+            mlb[(warp * 8 + 2 * t) * 2 + 0] = m_run[0];
+            mlb[(warp * 8 + 2 * t) * 2 + 1] = l_run[0];
+            mlb[(warp * 8 + 2 * t + 1) * 2 + 0] = m_run[1];
+            mlb[(warp * 8 + 2 * t + 1) * 2 + 1] = l_run[1];
+        }
+    }
+    __syncthreads();
+    const int d = threadIdx.x;  // 128 threads == 128 dims
+    for (int hh = 0; hh < c.G; ++hh) {
+        float M = NEG_INF;
+#pragma unroll
+        for (int w = 0; w < G_WARPS; ++w) M = fmaxf(M, mlb[(w * 8 + hh) * 2]);
+        float L = 0.f, O = 0.f;
+        if (M != NEG_INF) {
+#pragma unroll
+            for (int w = 0; w < G_WARPS; ++w) {
+                const float f = ex2(mlb[(w * 8 + hh) * 2] - M);
+                L += f * mlb[(w * 8 + hh) * 2 + 1];
+                O += f * ob[(w * 8 + hh) * GD + d];
+            }
+        }
+        if (a.splits == 1) {
+            const float r = L > 0.f ? O / L : 0.f;
+            a.out[((size_t)b * c.Hq + (size_t)h * c.G + hh) * GD + d] = __float2bfloat16_rn(r);
+        } else {
+            const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + split) * c.G + hh;
+            a.part_o[pi * GD + d] = O;
+            if (d == 0) {
+                a.part_ml[pi * 2 + 0] = M;
+                a.part_ml[pi * 2 + 1] = L;
+            }
+        }
+    }
+}
+
+// ===================================================================== MLA
+// Key row = [latent 512 | rope 64]; value = latent.  One CTA: 16 query heads of
+// one sequence over a range of 64-key tiles.  Warp w computes the scores of keys
+// 16w..16w+15 (all 576 columns); the softmax runs on shared memory; warp w then
+// accumulates O[:, 128w : 128w+128] = P V.
+constexpr int MK = 576, MV = 512;
+constexpr int M_ROWB = MK * 2;                        // 1152 bytes
+constexpr int M_STAGES = 2;
+constexpr int M_TILE_BYTES = MLA_KEYS * M_ROWB;       // 72 KB
+constexpr int M_Q_BYTES = MLA_HB * M_ROWB;            // 18 KB
+constexpr int M_S_BYTES = MLA_HB * MLA_KEYS * 4;      // 4 KB scores
+constexpr int M_P_BYTES = MLA_HB * MLA_KEYS * 2;      // 2 KB probabilities (bf16)
+constexpr int M_SMEM = M_STAGES * M_TILE_BYTES + M_Q_BYTES + M_S_BYTES + M_P_BYTES + 3 * MLA_HB * 4;
+
+__global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const DevConfig& c = a.cfg;
+    const int hb = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slot = a.slots[b];
+    if (slot < 0 || slot >= c.max_batch) {
+        if (tid == 0 && split == 0 && hb == 0) report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
+        if (a.splits == 1)
+            for (int i = tid; i < MLA_HB * MV; i += blockDim.x)
+                a.out[((size_t)b * c.Hq + (size_t)hb * MLA_HB) * MV + i] = __float2bfloat16_rn(0.f);
+        return;
+    }
+    const snap_seq_meta m = a.meta[slot];
+    SlotValidity sv;
+    sv.init(m, c);
+    const bf16* kvbase = a.kc + (size_t)slot * c.C * MK;
+
+    const uint32_t s_kv = smem_u32(smem);
+    const uint32_t s_q = s_kv + M_STAGES * M_TILE_BYTES;
+    float* S = reinterpret_cast<float*>(smem + M_STAGES * M_TILE_BYTES + M_Q_BYTES);
+    const uint32_t s_p = s_q + M_Q_BYTES + M_S_BYTES;
+    float* m_s = reinterpret_cast<float*>(smem + M_STAGES * M_TILE_BYTES + M_Q_BYTES + M_S_BYTES + M_P_BYTES);
+    float* l_s = m_s + MLA_HB;
+    float* al_s = l_s + MLA_HB;
+
+    // Q block -> shared (swizzled rows of 72 chunks)
+    {
+        const bf16* qp = a.q + ((size_t)b * c.Hq + (size_t)hb * MLA_HB) * MK;
+        for (int i = tid; i < MLA_HB * 72; i += 128) {
+            const int r = i / 72, ch = i % 72;
+            cp_async16(s_q + swz(r, ch, M_ROWB), qp + (size_t)r * MK + ch * 8);
+        }
+        cp_async_commit();
+    }
+    if (tid < MLA_HB) {
+        m_s[tid] = NEG_INF;
+        l_s[tid] = 0.f;
+    }
+
+    const int ntiles = (c.C + MLA_KEYS - 1) / MLA_KEYS;
+    const int t_begin = split * a.tiles_per_split;
+    const int t_end = min(ntiles, t_begin + a.tiles_per_split);
+    auto next_tile = [&](int t) {
+        while (t < t_end && !sv.any_valid(t * MLA_KEYS, min(c.C, (t + 1) * MLA_KEYS))) ++t;
+        return t;
+    };
+    auto load_tile = [&](int t, int st) {
+        const uint32_t dst = s_kv + st * M_TILE_BYTES;
+        for (int i = tid; i < MLA_KEYS * 72; i += 128) {
+            const int r = i / 72, ch = i % 72;
+            const int key = t * MLA_KEYS + r;
+            const bool ok = key < c.C;
+            cp_async16(dst + swz(r, ch, M_ROWB), kvbase + (size_t)(ok ? key : 0) * MK + ch * 8,
+                       ok ? 16 : 0);
+        }
+    };
+
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    int t_load = next_tile(t_begin), t_comp = t_load;
+    if (t_load < t_end) {
+        load_tile(t_load, 0);
+        t_load = next_tile(t_load + 1);
+    }
+    cp_async_commit();
+    int st = 0;
+    const float sl2 = c.scale_log2;
+    while (t_comp < t_end) {
+        if (t_load < t_end) {
+            load_tile(t_load, st ^ 1);
+            t_load = next_tile(t_load + 1);
+        }
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const uint32_t kv = s_kv + st * M_TILE_BYTES;
+        // ---- scores S[16 heads][keys 16w .. 16w+15]
+        {
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 4
+            for (int ks = 0; ks < MK / 16; ++ks) {
+                uint32_t af[4], bfr[4];
+                const int ar = (lane & 7) + (((lane >> 3) & 1) << 3);
+                ldsm_x4(s_q + swz(ar, ks * 2 + (lane >> 4), M_ROWB), af[0], af[1], af[2], af[3]);
+                const int br = warp * 16 + (lane & 7) + ((lane >> 4) << 3);
+                ldsm_x4(kv + swz(br, ks * 2 + ((lane >> 3) & 1), M_ROWB), bfr[0], bfr[1], bfr[2], bfr[3]);
+                mma_bf16(acc[0], af, bfr[0], bfr[1]);
+                mma_bf16(acc[1], af, bfr[2], bfr[3]);
+            }
+            const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int kl = warp * 16 + nt * 8 + 2 * t + (i & 1);
+                    const int row = g + 8 * (i >> 1);
+                    const int key = t_comp * MLA_KEYS + kl;
+                    const bool ok = key < c.C && sv.valid(key);
+                    S[row * MLA_KEYS + kl] = ok ? acc[nt][i] * sl2 : NEG_INF;
+                }
+        }
+        __syncthreads();
+        // ---- online softmax: thread = (row tid/8, 8 keys)
+        {
+            const int row = tid >> 3, seg = tid & 7;
+            float v[8];
+            float mx = NEG_INF;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[i] = S[row * MLA_KEYS + seg * 8 + i];
+                mx = fmaxf(mx, v[i]);
+            }
+#pragma unroll
+            for (int x = 1; x < 8; x <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
+            const float mo = m_s[row];
+            const float mn = fmaxf(mo, mx);
+            const float al = mn == NEG_INF ? 1.f : ex2(mo - mn);
+            float sum = 0.f;
+            uint32_t pk[4];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const float p0 = mn == NEG_INF ? 0.f : bf16_round(ex2(v[i] - mn));
+                const float p1 = mn == NEG_INF ? 0.f : bf16_round(ex2(v[i + 1] - mn));
+                sum += p0 + p1;
+                pk[i / 2] = pack_bf16(p0, p1);
+            }
+#pragma unroll
+            for (int x = 1; x < 8; x <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, x);
+            const uint32_t dst = s_p + swz(row, seg, MLA_KEYS * 2);
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst), "r"(pk[0]), "r"(pk[1]),
+                         "r"(pk[2]), "r"(pk[3]));
+            __syncwarp();
+            if (seg == 0) {
+                m_s[row] = mn;
+                l_s[row] = l_s[row] * al + sum;
+                al_s[row] = al;
+            }
+        }
+        __syncthreads();
+        // ---- O[:, 128w : 128w+128] = O * alpha + P V
+        {
+            const int g = lane >> 2;
+            const float a0 = al_s[g], a1 = al_s[g + 8];
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+                o[nt][0] *= a0;
+                o[nt][1] *= a0;
+                o[nt][2] *= a1;
+                o[nt][3] *= a1;
+            }
+#pragma unroll
+            for (int ks = 0; ks < MLA_KEYS / 16; ++ks) {
+                uint32_t af[4];
+                const int ar = (lane & 7) + (((lane >> 3) & 1) << 3);
+                ldsm_x4(s_p + swz(ar, ks * 2 + (lane >> 4), MLA_KEYS * 2), af[0], af[1], af[2], af[3]);
+#pragma unroll
+                for (int nt = 0; nt < 16; nt += 2) {
+                    uint32_t bfr[4];
+                    const int key = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                    const int ch = warp * 16 + nt + (lane >> 4);
+                    ldsm_x4_t(kv + swz(key, ch, M_ROWB), bfr[0], bfr[1], bfr[2], bfr[3]);
+                    mma_bf16(o[nt], af, bfr[0], bfr[1]);
+                    mma_bf16(o[nt + 1], af, bfr[2], bfr[3]);
+                }
+            }
+        }
+        __syncthreads();  // stage and S/P buffers are reused next iteration
+        t_comp = next_tile(t_comp + 1);
+        st ^= 1;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // write this split's result
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int row = g + 8 * (i >> 1);
+            const int d = warp * 128 + nt * 8 + 2 * t + (i & 1);
+            const int head = hb * MLA_HB + row;
+            if (a.splits == 1) {
+                const float L = l_s[row];
+                const float r = L > 0.f ? o[nt][i] / L : 0.f;
+                a.out[((size_t)b * c.Hq + head) * MV + d] = __float2bfloat16_rn(r);
+            } else {
+                const size_t pi = ((size_t)b * a.splits + split) * c.Hq + head;
+                a.part_o[pi * MV + d] = o[nt][i];
+            }
+        }
+    if (a.splits > 1 && tid < MLA_HB) {
+        const size_t pi = ((size_t)b * a.splits + split) * c.Hq + hb * MLA_HB + tid;
+        a.part_ml[pi * 2 + 0] = m_s[tid];
+        a.part_ml[pi * 2 + 1] = l_s[tid];
+    }
+}
+
+// =================================================================== merge
+// out[b][i][:] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s  (zero if empty).
+// Partial index: ((b * Hkv + h) * splits + s) * G + hh  for query head i = h*G + hh.
+__global__ void decode_merge_kernel(DecodeArgs a) {
+    const DevConfig& c = a.cfg;
+    const int i = blockIdx.x, b = blockIdx.y;
+    const int h = i / c.G, hh = i % c.G;
+    const int slot = a.slots[b];
+    const bool ok = slot >= 0 && slot < c.max_batch;
+    float M = NEG_INF;
+    if (ok)
+        for (int s = 0; s < a.splits; ++s) {
+            const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + s) * c.G + hh;
+            M = fmaxf(M, a.part_ml[pi * 2]);
+        }
+    float L = 0.f;
+    if (M != NEG_INF)
+        for (int s = 0; s < a.splits; ++s) {
+            const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + s) * c.G + hh;
+            L += ex2(a.part_ml[pi * 2] - M) * a.part_ml[pi * 2 + 1];
+        }
+    for (int d = threadIdx.x; d < c.dv; d += blockDim.x) {
+        float O = 0.f;
+        if (M != NEG_INF)
+            for (int s = 0; s < a.splits; ++s) {
+                const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + s) * c.G + hh;
+                O += ex2(a.part_ml[pi * 2] - M) * a.part_o[pi * c.dv + d];
+            }
+        a.out[((size_t)b * c.Hq + i) * c.dv + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(gqa_decode_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid(a.splits, a.cfg.Hkv, a.n);
+    gqa_decode_kernel<<<grid, G_WARPS * 32, G_SMEM, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_mla(const DecodeArgs& a, cudaStream_t st) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, M_SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid(a.cfg.Hq / MLA_HB, a.splits, a.n);
+    mla_decode_kernel<<<grid, 128, M_SMEM, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st) {
+    dim3 grid(a.cfg.Hq, a.n);
+    decode_merge_kernel<<<grid, 128, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace snap

@@ -1,0 +1,85 @@
+// kernels.cuh -- launch interfaces between the C-ABI layer and the kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace snap {
+
+using bf16 = __nv_bfloat16;
+
+// ----------------------------------------------------------------- decode
+struct DecodeArgs {
+    const bf16* kc;              // cache keys   [max_batch][Hkv][C][dqk]
+    const bf16* vc;              // cache values [max_batch][Hkv][C][dv] (GQA)
+    const snap_seq_meta* meta;   // [max_batch]
+    const int32_t* slots;        // [n]
+    int n;
+    const bf16* q;               // [n][Hq][dqk]
+    bf16* out;                   // [n][Hq][dv]
+    float* part_o;               // [n][Hkv][splits][G][dv]
+    float* part_ml;              // [n][Hkv][splits][G][2]  (max, sum) base-2 domain
+    int splits;
+    int tiles_per_split;         // in units of the kernel's key tile
+    int32_t* status;
+    DevConfig cfg;
+};
+
+constexpr int GQA_KEYS = 32;     // keys per warp step of the GQA decode kernel
+constexpr int MLA_KEYS = 64;     // keys per CTA step of the MLA decode kernel
+constexpr int MLA_HB = 16;       // query heads per MLA CTA
+
+cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_mla(const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st);
+
+// ----------------------------------------------------------------- append
+struct AppendArgs {
+    bf16* kc;
+    bf16* vc;
+    snap_seq_meta* meta;
+    const int32_t* slots;
+    int n;
+    const bf16* k_new;           // [n][Hkv][dqk]
+    const bf16* v_new;           // [n][Hkv][dv]
+    int32_t* status;
+    DevConfig cfg;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
+
+// --------------------------------------------------------------- compress
+struct CompressArgs {
+    const bf16* K;               // prompt keys (strided)
+    const bf16* V;               // prompt values (GQA)
+    int64_t tok_stride, head_stride;   // elements
+    const bf16* Q;               // [W][Hq][dqk]
+    int S;
+    int R;                       // G * W observation rows per KV head
+    int R0, n_sink, n_mid;
+    int scored;                  // 1 when the SnapKV selection runs
+    int slot;
+    // workspace
+    float* part_ml;              // [Hkv][R][row_splits][2]
+    float* lse2;                 // [Hkv][R]
+    float* col;                  // [Hkv][S_pad]
+    uint32_t* pool;              // [Hkv][S_pad] pooled score bits
+    int row_splits;
+    int64_t S_pad;
+    // cache
+    bf16* kc;
+    bf16* vc;
+    snap_seq_meta* meta;
+    int32_t* sel;                // [max_batch][Hkv][K]
+    int32_t* status;
+    DevConfig cfg;
+};
+
+constexpr int CMP_KEYS = 64;     // keys per tile in the score passes
+constexpr int CMP_ROWS = 64;     // observation rows per tile in the score passes
+
+cudaError_t launch_rowstat(const CompressArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_lse_merge(const CompressArgs& a, cudaStream_t st);
+cudaError_t launch_colsum(const CompressArgs& a, int num_sms, cudaStream_t st);
+cudaError_t launch_select(const CompressArgs& a, cudaStream_t st);
+cudaError_t launch_cache_write(const CompressArgs& a, int num_sms, cudaStream_t st);
+
+}  // namespace snap

@@ -1,0 +1,403 @@
+// snap_api.cu -- the C ABI of libsnap (see include/snap.h): argument checks,
+// cache/workspace layout, and the launch sequence of each entry point.
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "kernels.cuh"
+
+using namespace snap;
+
+struct snap_cache {
+    snap_config cfg;
+    int max_batch;
+    int64_t C;
+    void* base;
+    size_t bytes;
+    bf16* k;
+    bf16* v;
+    snap_seq_meta* meta;
+    int32_t* sel;
+    int32_t* status;
+};
+
+namespace {
+
+constexpr int ABI_VERSION = 1;
+constexpr int MAX_ROW_SPLITS = 64;
+constexpr int MAX_DECODE_SPLITS = 32;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms() {
+    static int cached = 0;
+    if (cached == 0) {
+        int dev = 0, n = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+            cached = n;
+        else
+            return 148;
+    }
+    return cached;
+}
+
+DevConfig dev_config(const snap_config& c, int max_batch) {
+    DevConfig d;
+    d.layout = c.layout;
+    d.Hq = c.n_q_heads;
+    d.Hkv = c.n_kv_heads;
+    d.G = c.n_q_heads / c.n_kv_heads;
+    d.dqk = c.d_qk;
+    d.dv = c.d_v;
+    d.L_sink = c.L_sink;
+    d.K = c.K;
+    d.L_recent = c.L_recent;
+    d.W = c.W;
+    d.P = c.P;
+    d.C = c.L_sink + c.K + c.L_recent;
+    d.max_batch = max_batch;
+    d.scale = c.sm_scale;
+    d.scale_log2 = c.sm_scale * 1.4426950408889634f;
+    return d;
+}
+
+struct CacheRegions {
+    size_t meta, status, sel, k, v, total;
+};
+
+CacheRegions regions(const snap_config& c, int max_batch) {
+    const size_t C = (size_t)c.L_sink + c.K + c.L_recent;
+    CacheRegions r;
+    size_t off = 0;
+    r.meta = off;
+    off = align_up(off + sizeof(snap_seq_meta) * max_batch, 256);
+    r.status = off;
+    off = align_up(off + 16, 256);
+    r.sel = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)max_batch * c.n_kv_heads * c.K, 256);
+    r.k = off;
+    off = align_up(off + 2 * (size_t)max_batch * c.n_kv_heads * C * c.d_qk, 256);
+    r.v = off;
+    if (c.layout == SNAP_LAYOUT_GQA) off = align_up(off + 2 * (size_t)max_batch * c.n_kv_heads * C * c.d_v, 256);
+    r.total = off;
+    return r;
+}
+
+// Compress workspace regions for a prompt of S tokens.
+struct CompressWs {
+    size_t part_ml, lse2, col, pool, total;
+    int64_t S_pad;
+};
+
+CompressWs compress_ws(const snap_config& c, int64_t S) {
+    const int G = c.n_q_heads / c.n_kv_heads;
+    const size_t R = (size_t)G * c.W;
+    CompressWs w;
+    w.S_pad = (S + 63) / 64 * 64;
+    size_t off = 0;
+    w.part_ml = off;
+    off = align_up(off + sizeof(float) * 2 * c.n_kv_heads * R * MAX_ROW_SPLITS, 256);
+    w.lse2 = off;
+    off = align_up(off + sizeof(float) * c.n_kv_heads * R, 256);
+    w.col = off;
+    off = align_up(off + sizeof(float) * c.n_kv_heads * (size_t)w.S_pad, 256);
+    w.pool = off;
+    off = align_up(off + sizeof(uint32_t) * c.n_kv_heads * (size_t)w.S_pad, 256);
+    w.total = off;
+    return w;
+}
+
+size_t decode_ws_bytes(const snap_config& c, int max_n) {
+    const size_t parts = (size_t)max_n * c.n_q_heads * MAX_DECODE_SPLITS;
+    return align_up(parts * sizeof(float) * c.d_v, 256) + align_up(parts * sizeof(float) * 2, 256);
+}
+
+snap_status check_config(const snap_config* c) {
+    if (!c) return SNAP_ERR_INVALID_ARG;
+    if (c->layout != SNAP_LAYOUT_GQA && c->layout != SNAP_LAYOUT_MLA) return SNAP_ERR_SHAPE;
+    if (c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->n_q_heads % c->n_kv_heads) return SNAP_ERR_SHAPE;
+    if (c->d_qk <= 0 || c->d_v <= 0) return SNAP_ERR_SHAPE;
+    if (c->L_sink < 0 || c->K < 0 || c->L_recent < 1) return SNAP_ERR_SHAPE;
+    if (c->W < 1 || c->W > c->L_recent) return SNAP_ERR_SHAPE;
+    if (c->P < 1 || c->P % 2 == 0) return SNAP_ERR_SHAPE;
+    if (!(c->sm_scale > 0.f)) return SNAP_ERR_SHAPE;
+    if ((int64_t)c->L_sink + c->K + c->L_recent > (1ll << 30)) return SNAP_ERR_SHAPE;
+    if (c->layout == SNAP_LAYOUT_MLA) {
+        if (c->n_kv_heads != 1 || c->d_v > c->d_qk) return SNAP_ERR_SHAPE;
+        if (c->d_qk != 576 || c->d_v != 512 || c->n_q_heads % MLA_HB) return SNAP_ERR_UNSUPPORTED;
+    } else {
+        if (c->d_qk != 128 || c->d_v != 128) return SNAP_ERR_UNSUPPORTED;
+        if (c->n_q_heads / c->n_kv_heads > 8) return SNAP_ERR_UNSUPPORTED;
+    }
+    return SNAP_OK;
+}
+
+snap_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return SNAP_OK;
+    std::fprintf(stderr, "libsnap: CUDA error %s\n", cudaGetErrorString(e));
+    return SNAP_ERR_CUDA;
+}
+
+// Split count for decode: enough CTAs for several full waves, never more splits
+// than tiles, and each split at least 4 tiles.
+int decode_splits(int base, int tiles, int ctas_per_sm) {
+    const int wave = num_sms() * ctas_per_sm;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int s = 1; s <= MAX_DECODE_SPLITS; ++s) {
+        if (s > 1 && (tiles + s - 1) / s < 4) break;
+        const long long ctas = (long long)base * s;
+        const long long waves = (ctas + wave - 1) / wave;
+        double eff = (double)ctas / (double)(waves * wave);
+        // prefer more parallelism until two waves are covered
+        if (ctas < 2 * wave) eff *= (double)ctas / (2.0 * wave);
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = s;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* snap_status_string(int s) {
+    switch (s) {
+        case SNAP_OK: return "ok";
+        case SNAP_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad count)";
+        case SNAP_ERR_SHAPE: return "shape violates the method's preconditions";
+        case SNAP_ERR_UNSUPPORTED: return "configuration not supported by these kernels";
+        case SNAP_ERR_CUDA: return "CUDA call failed";
+        case SNAP_ERR_TIMEOUT: return "a kernel's bounded wait expired";
+        case SNAP_ERR_DEVICE_CHECK: return "a kernel rejected an index (slot out of range)";
+        default: return "unknown status";
+    }
+}
+
+int snap_abi_version(void) { return ABI_VERSION; }
+
+snap_status snap_config_check(const snap_config* cfg) { return check_config(cfg); }
+
+snap_status snap_cache_bytes(const snap_config* cfg, int max_batch, size_t* bytes) {
+    snap_status s = check_config(cfg);
+    if (s != SNAP_OK) return s;
+    if (max_batch < 1 || !bytes) return SNAP_ERR_INVALID_ARG;
+    *bytes = regions(*cfg, max_batch).total;
+    return SNAP_OK;
+}
+
+snap_status snap_cache_create(const snap_config* cfg, int max_batch, void* dev_buf, size_t bytes,
+                              void* stream, snap_cache** out) {
+    snap_status s = check_config(cfg);
+    if (s != SNAP_OK) return s;
+    if (max_batch < 1 || !dev_buf || !out) return SNAP_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(dev_buf) & 255u) return SNAP_ERR_INVALID_ARG;
+    const CacheRegions r = regions(*cfg, max_batch);
+    if (bytes < r.total) return SNAP_ERR_INVALID_ARG;
+    snap_cache* c = new (std::nothrow) snap_cache;
+    if (!c) return SNAP_ERR_INVALID_ARG;
+    uint8_t* base = static_cast<uint8_t*>(dev_buf);
+    c->cfg = *cfg;
+    c->max_batch = max_batch;
+    c->C = (int64_t)cfg->L_sink + cfg->K + cfg->L_recent;
+    c->base = dev_buf;
+    c->bytes = bytes;
+    c->meta = reinterpret_cast<snap_seq_meta*>(base + r.meta);
+    c->status = reinterpret_cast<int32_t*>(base + r.status);
+    c->sel = reinterpret_cast<int32_t*>(base + r.sel);
+    c->k = reinterpret_cast<bf16*>(base + r.k);
+    c->v = cfg->layout == SNAP_LAYOUT_GQA ? reinterpret_cast<bf16*>(base + r.v) : nullptr;
+    cudaError_t e = cudaMemsetAsync(dev_buf, 0, r.total, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        delete c;
+        return cuda_status(e);
+    }
+    *out = c;
+    return SNAP_OK;
+}
+
+void snap_cache_destroy(snap_cache* cache) { delete cache; }
+
+snap_status snap_cache_view_get(const snap_cache* cache, snap_cache_view* out) {
+    if (!cache || !out) return SNAP_ERR_INVALID_ARG;
+    out->k = cache->k;
+    out->v = cache->v;
+    out->meta = cache->meta;
+    out->sel = cache->sel;
+    out->status = cache->status;
+    out->C = cache->C;
+    out->max_batch = cache->max_batch;
+    return SNAP_OK;
+}
+
+snap_status snap_compress_ws_bytes(const snap_config* cfg, int64_t S_max, size_t* bytes) {
+    snap_status s = check_config(cfg);
+    if (s != SNAP_OK) return s;
+    if (S_max < 1 || !bytes) return SNAP_ERR_INVALID_ARG;
+    *bytes = compress_ws(*cfg, S_max).total;
+    return SNAP_OK;
+}
+
+snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
+                          int64_t tok_stride, int64_t head_stride, const void* Q_obs, void* ws,
+                          size_t ws_bytes, void* stream) {
+    if (!cache || !K || !Q_obs) return SNAP_ERR_INVALID_ARG;
+    const snap_config& c = cache->cfg;
+    if (slot < 0 || slot >= cache->max_batch) return SNAP_ERR_INVALID_ARG;
+    if (S < 1 || S > (1ll << 30)) return SNAP_ERR_SHAPE;
+    if (c.layout == SNAP_LAYOUT_GQA && !V) return SNAP_ERR_INVALID_ARG;
+    if (c.layout == SNAP_LAYOUT_MLA && V) return SNAP_ERR_INVALID_ARG;
+    if (!aligned16(K) || (V && !aligned16(V)) || !aligned16(Q_obs)) return SNAP_ERR_INVALID_ARG;
+    if (tok_stride < 0 || head_stride < 0 || (tok_stride * 2) % 16 || (head_stride * 2) % 16)
+        return SNAP_ERR_INVALID_ARG;
+    if (c.n_kv_heads > 1 && head_stride < c.d_qk) return SNAP_ERR_INVALID_ARG;
+    if (S > 1 && tok_stride < c.d_qk) return SNAP_ERR_INVALID_ARG;
+
+    const int64_t n_sink = S < c.L_sink ? S : c.L_sink;
+    int64_t R0 = S <= c.L_sink ? S : (S - c.L_recent > c.L_sink ? S - c.L_recent : c.L_sink);
+    const int64_t M = R0 - n_sink;
+    const int64_t n_mid = M < c.K ? M : c.K;
+    const bool scored = M > c.K && c.K > 0;
+
+    CompressArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.K = static_cast<const bf16*>(K);
+    a.V = static_cast<const bf16*>(V);
+    a.tok_stride = tok_stride;
+    a.head_stride = head_stride;
+    a.Q = static_cast<const bf16*>(Q_obs);
+    a.S = (int)S;
+    a.R = (c.n_q_heads / c.n_kv_heads) * c.W;
+    a.R0 = (int)R0;
+    a.n_sink = (int)n_sink;
+    a.n_mid = (int)n_mid;
+    a.scored = scored ? 1 : 0;
+    a.slot = slot;
+    a.kc = cache->k;
+    a.vc = cache->v;
+    a.meta = cache->meta;
+    a.sel = cache->sel;
+    a.status = cache->status;
+    a.cfg = dev_config(c, cache->max_batch);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (scored) {
+        const CompressWs w = compress_ws(c, S);
+        if (!ws || ws_bytes < w.total) return SNAP_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(ws) & 255u) return SNAP_ERR_INVALID_ARG;
+        uint8_t* wb = static_cast<uint8_t*>(ws);
+        a.part_ml = reinterpret_cast<float*>(wb + w.part_ml);
+        a.lse2 = reinterpret_cast<float*>(wb + w.lse2);
+        a.col = reinterpret_cast<float*>(wb + w.col);
+        a.pool = reinterpret_cast<uint32_t*>(wb + w.pool);
+        a.S_pad = w.S_pad;
+        // row splits: about two waves of rowstat CTAs
+        const int row_blocks = (a.R + CMP_ROWS - 1) / CMP_ROWS;
+        const int per_sm = c.d_qk == 128 ? 4 : 1;
+        const int nkt = (int)((S + CMP_KEYS - 1) / CMP_KEYS);
+        int rs = (2 * num_sms() * per_sm + row_blocks * c.n_kv_heads - 1) / (row_blocks * c.n_kv_heads);
+        if (rs > MAX_ROW_SPLITS) rs = MAX_ROW_SPLITS;
+        if (rs > nkt) rs = nkt;
+        if (rs < 1) rs = 1;
+        a.row_splits = rs;
+        cudaError_t e = launch_rowstat(a, num_sms(), st);
+        if (e == cudaSuccess) e = launch_lse_merge(a, st);
+        if (e == cudaSuccess) e = launch_colsum(a, num_sms(), st);
+        if (e == cudaSuccess) e = launch_select(a, st);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return cuda_status(launch_cache_write(a, num_sms(), st));
+}
+
+snap_status snap_decode_append(snap_cache* cache, const int32_t* slots, int n, const void* k_new,
+                               const void* v_new, void* stream) {
+    if (!cache || n < 0) return SNAP_ERR_INVALID_ARG;
+    if (n == 0) return SNAP_OK;
+    if (!slots || !k_new || !aligned16(k_new)) return SNAP_ERR_INVALID_ARG;
+    const snap_config& c = cache->cfg;
+    if (c.layout == SNAP_LAYOUT_GQA && (!v_new || !aligned16(v_new))) return SNAP_ERR_INVALID_ARG;
+    if (c.layout == SNAP_LAYOUT_MLA && v_new) return SNAP_ERR_INVALID_ARG;
+    if (n > cache->max_batch) return SNAP_ERR_INVALID_ARG;
+    AppendArgs a;
+    a.kc = cache->k;
+    a.vc = cache->v;
+    a.meta = cache->meta;
+    a.slots = slots;
+    a.n = n;
+    a.k_new = static_cast<const bf16*>(k_new);
+    a.v_new = static_cast<const bf16*>(v_new);
+    a.status = cache->status;
+    a.cfg = dev_config(c, cache->max_batch);
+    return cuda_status(launch_append(a, static_cast<cudaStream_t>(stream)));
+}
+
+snap_status snap_decode_attn_ws_bytes(const snap_config* cfg, int max_n, size_t* bytes) {
+    snap_status s = check_config(cfg);
+    if (s != SNAP_OK) return s;
+    if (max_n < 1 || !bytes) return SNAP_ERR_INVALID_ARG;
+    *bytes = decode_ws_bytes(*cfg, max_n);
+    return SNAP_OK;
+}
+
+snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, const void* q,
+                             void* out, void* ws, size_t ws_bytes, void* stream) {
+    if (!cache || n < 0) return SNAP_ERR_INVALID_ARG;
+    if (n == 0) return SNAP_OK;
+    if (!slots || !q || !out || !aligned16(q) || !aligned16(out)) return SNAP_ERR_INVALID_ARG;
+    if (n > cache->max_batch) return SNAP_ERR_INVALID_ARG;
+    const snap_config& c = cache->cfg;
+    DecodeArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.kc = cache->k;
+    a.vc = cache->v;
+    a.meta = cache->meta;
+    a.slots = slots;
+    a.n = n;
+    a.q = static_cast<const bf16*>(q);
+    a.out = static_cast<bf16*>(out);
+    a.status = cache->status;
+    a.cfg = dev_config(c, cache->max_batch);
+    const int key_tile = c.layout == SNAP_LAYOUT_GQA ? GQA_KEYS : MLA_KEYS;
+    const int tiles = (int)((cache->C + key_tile - 1) / key_tile);
+    const int base = c.layout == SNAP_LAYOUT_GQA ? n * c.n_kv_heads : n * (c.n_q_heads / MLA_HB);
+    // GQA: each split is walked by 4 warps, one 32-key tile each per step
+    int splits = decode_splits(base, c.layout == SNAP_LAYOUT_GQA ? tiles / 4 : tiles, 1);
+    a.splits = splits;
+    a.tiles_per_split = (tiles + splits - 1) / splits;
+    if (splits > 1) {
+        const size_t need = decode_ws_bytes(c, n);
+        if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SNAP_ERR_INVALID_ARG;
+        const size_t parts = (size_t)n * c.n_q_heads * MAX_DECODE_SPLITS;
+        a.part_o = static_cast<float*>(ws);
+        a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align_up(parts * sizeof(float) * c.d_v, 256));
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = c.layout == SNAP_LAYOUT_GQA ? launch_decode_gqa(a, st) : launch_decode_mla(a, st);
+    if (e == cudaSuccess && splits > 1) e = launch_decode_merge(a, st);
+    return cuda_status(e);
+}
+
+snap_status snap_check_device(snap_cache* cache, void* stream) {
+    if (!cache) return SNAP_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t h[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaMemcpyAsync(h, cache->status, sizeof h, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (h[0] != 0) {
+        std::fprintf(stderr, "libsnap: device status %d (%s) detail %d %d %d\n", h[0], snap_status_string(h[0]),
+                     h[1], h[2], h[3]);
+        e = cudaMemsetAsync(cache->status, 0, sizeof h, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_status(e);
+        return static_cast<snap_status>(h[0]);
+    }
+    return SNAP_OK;
+}
+
+}  // extern "C"

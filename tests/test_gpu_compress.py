@@ -1,0 +1,124 @@
+"""GPU parity of snap_compress (prefill compression) against the CPU oracle.
+
+SnapStream episode companion page, "Fixed-Size Cache Layout": sinks + SnapKV
+top-K middle + recent window, built once at prefill.  Each case runs the CUDA
+library through its C ABI and the oracle on the same seeded inputs, then checks
+the meta exactly, the selection up to ties within 1e-6 relative, and every cache
+row bit-exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fixed_size_kv_gb300 import inputs, snap
+from parity import (check_cache_rows, check_selection, gpu_meta, oracle_cfg, snap_cfg)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_compress(wl, S, seed, slot=0, max_batch=2, want_pool=True, strided=False):
+    pre = inputs.gen_prefill(wl, S, seed=seed)
+    cache = snap.SnapCache(snap_cfg(wl), max_batch=max_batch, max_prompt=S)
+    K, V = pre.K.cuda(), (pre.V.cuda() if pre.V is not None else None)
+    if strided:
+        # K and V as views into one [S][2][H_kv][d] prefill buffer (non-contiguous tokens)
+        kv = torch.stack([K, V], dim=1)
+        K, V = kv[:, 0], kv[:, 1]
+    cache.compress(slot, K, V, pre.Q.cuda())
+    torch.cuda.synchronize()
+    assert cache.check_device() == snap.SNAP_OK
+    ocache = oracle.compress(oracle_cfg(wl), pre.K, pre.V, pre.Q, want_pool=want_pool)
+    return pre, cache, ocache
+
+
+def check_all(wl, pre, cache, ocache, slot=0, where=""):
+    swaps = 0
+    if ocache.pool is not None and ocache.meta.n_mid == wl.K and wl.K > 0 and \
+            ocache.meta.R0 - ocache.meta.n_sink > wl.K:
+        gsel = cache.selected()[slot].cpu().numpy()
+        for h in range(wl.n_kv_heads):
+            swaps += check_selection(gsel[h], ocache.sel[h], ocache.pool[h], f"{where} head {h}")
+    else:
+        if wl.K > 0:
+            np.testing.assert_array_equal(cache.selected()[slot].cpu().numpy(), ocache.sel)
+    check_cache_rows(cache, slot, ocache, pre.K, pre.V, where)
+    return swaps
+
+
+def small_gqa(**kw):
+    base = dict(name="small", layout=0, n_q_heads=32, n_kv_heads=8, d_qk=128, d_v=128,
+                L_sink=4, K=60, L_recent=64, W=16, P=7, batch=1, prompt_min=0, prompt_max=0,
+                decode_steps=0, sm_scale=1 / math.sqrt(128))
+    base.update(kw)
+    return inputs.Workload(**base)
+
+
+def test_compress_tiny_config_exact():
+    """Llama-3.1-8B shape, 2048-token prompt, cache 4 + 252 + 256 (the smallest workload)."""
+    wl = inputs.WORKLOADS["gqa_2k_tiny"]
+    pre, cache, ocache = run_compress(wl, 2048, seed=0, slot=1)
+    swaps = check_all(wl, pre, cache, ocache, slot=1, where="gqa_2k_tiny")
+    assert swaps <= 2
+
+
+@pytest.mark.parametrize("S", [2048 + 37, 1000, 777])
+def test_compress_ragged_lengths(S):
+    """Prompt lengths that are not a multiple of any tile (ragged tails)."""
+    wl = inputs.WORKLOADS["gqa_2k_tiny"]
+    pre, cache, ocache = run_compress(wl, S, seed=S)
+    check_all(wl, pre, cache, ocache, where=f"S={S}")
+
+
+@pytest.mark.parametrize("case", [
+    dict(S=3),                                # shorter than the sinks
+    dict(S=4),                                # exactly the sinks
+    dict(S=50),                               # sinks + ring, no middle
+    dict(S=68),                               # ring just full, no middle
+    dict(S=128),                              # middle holds exactly K = 60
+    dict(S=129),                              # one too many: scoring runs
+    dict(S=300, K=0),                         # StreamingLLM only (no middle)
+    dict(S=300, P=1),                         # no pooling
+    dict(S=300, W=1),                         # one observation query
+    dict(S=300, L_sink=0),                    # no sinks
+    dict(S=513, W=64, L_recent=64, K=100),    # window fills the whole ring
+])
+def test_compress_edge_cases(case):
+    case = dict(case)
+    S = case.pop("S")
+    wl = small_gqa(**case)
+    pre, cache, ocache = run_compress(wl, S, seed=7 + S)
+    check_all(wl, pre, cache, ocache, where=str(case))
+
+
+def test_compress_group_of_eight_and_strided_inputs():
+    """G = 8 query heads per KV head; K and V passed as strided views."""
+    wl = small_gqa(n_q_heads=16, n_kv_heads=2, W=8)
+    pre, cache, ocache = run_compress(wl, 900, seed=5, strided=True)
+    check_all(wl, pre, cache, ocache, where="G=8 strided")
+
+
+def test_compress_mla_small():
+    """DeepSeek MLA latent layout (576-wide key row, value = first 512 columns)."""
+    wl = inputs.Workload("mla_small", 1, 32, 1, 576, 512, 4, 40, 64, 8, 5, 1, 0, 0, 0,
+                         1 / math.sqrt(192))
+    pre, cache, ocache = run_compress(wl, 700, seed=11)
+    check_all(wl, pre, cache, ocache, where="mla small")
+
+
+def test_compress_reuses_slot_cleanly():
+    """A slot compressed twice holds only the second prompt (unused slots zeroed)."""
+    wl = small_gqa()
+    pre1 = inputs.gen_prefill(wl, 400, seed=1)
+    pre2 = inputs.gen_prefill(wl, 30, seed=2)
+    cache = snap.SnapCache(snap_cfg(wl), max_batch=1, max_prompt=400)
+    cache.compress(0, pre1.K.cuda(), pre1.V.cuda(), pre1.Q.cuda())
+    cache.compress(0, pre2.K.cuda(), pre2.V.cuda(), pre2.Q.cuda())
+    torch.cuda.synchronize()
+    ocache = oracle.compress(oracle_cfg(wl), pre2.K, pre2.V, pre2.Q)
+    check_cache_rows(cache, 0, ocache, pre2.K, pre2.V, "reused slot")
+    v = cache.k_cache()[0].float()
+    pos = ocache.slot_positions()
+    assert float(v[torch.from_numpy(pos < 0)].abs().sum()) == 0.0

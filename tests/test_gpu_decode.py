@@ -1,0 +1,158 @@
+"""GPU parity of snap_decode_append + snap_decode_attn against the CPU oracle.
+
+SnapStream episode companion page, "Ring Buffer vs. Naive Slicing": decode only
+rotates the recent window, scattering each new token into a fixed ring index;
+"Prefill / Decode Pipeline": decode streams the cache once per token.  Cases
+cover a continuous batch whose sequences sit at different ring offsets, partly
+filled caches, permuted slots, the full-KV baseline and the MLA latent layout.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fixed_size_kv_gb300 import inputs, snap
+from parity import (check_cache_rows, check_outputs, oracle_cache_from_gpu, oracle_cfg, snap_cfg)
+
+pytestmark = pytest.mark.gpu
+
+
+class Batch:
+    """Runs the GPU cache and the oracle caches side by side."""
+
+    def __init__(self, wl, lengths, slots, seed, max_batch=None):
+        self.wl = wl
+        self.slots = list(slots)
+        self.cache = snap.SnapCache(snap_cfg(wl), max_batch=max_batch or (max(slots) + 1),
+                                    max_prompt=max(lengths))
+        self.ocaches, self.K, self.V = [], [], []
+        for i, (S, slot) in enumerate(zip(lengths, slots)):
+            pre = inputs.gen_prefill(wl, S, seed=seed, seq=i)
+            self.cache.compress(slot, pre.K.cuda(), pre.V.cuda() if pre.V is not None else None,
+                                pre.Q.cuda())
+            self.ocaches.append(oracle.compress(oracle_cfg(wl), pre.K, pre.V, pre.Q))
+            self.K.append(pre.K)
+            self.V.append(pre.V)
+        torch.cuda.synchronize()
+        self.dslots = torch.tensor(self.slots, dtype=torch.int32, device="cuda")
+        self.seed = seed
+
+    def step(self, t, append=True, isolated=False):
+        wl, n = self.wl, len(self.slots)
+        tok = inputs.gen_decode(wl, n, step=t, seed=self.seed)
+        if append:
+            self.cache.decode_append(self.dslots, tok.k.cuda(), tok.v.cuda() if tok.v is not None else None)
+        out = self.cache.decode_attn(self.dslots, tok.q.cuda())
+        torch.cuda.synchronize()
+        assert self.cache.check_device() == snap.SNAP_OK
+        for i in range(n):
+            if append:
+                oracle.append(self.ocaches[i], tok.k[i], tok.v[i] if tok.v is not None else None)
+                self.K[i] = torch.cat([self.K[i], tok.k[i:i + 1]])
+                if tok.v is not None:
+                    self.V[i] = torch.cat([self.V[i], tok.v[i:i + 1]])
+            oc = self.ocaches[i]
+            if isolated:  # the oracle reads the GPU's own cache
+                oc = oracle_cache_from_gpu(self.cache, self.slots[i], oracle_cfg(wl))
+            check_outputs(out[i], oracle.decode_attn(oc, tok.q[i]), f"step {t} seq {i}")
+        return out
+
+    def check_rows(self):
+        for i, slot in enumerate(self.slots):
+            check_cache_rows(self.cache, slot, self.ocaches[i], self.K[i], self.V[i], f"seq {i}")
+
+
+def test_decode_tiny_config_64_steps():
+    """The 2048-token workload: 64 decode steps, every output and the final ring checked."""
+    wl = inputs.WORKLOADS["gqa_2k_tiny"]
+    b = Batch(wl, [2048], [0], seed=3)
+    b.step(0, append=False)  # attention right after compression
+    for t in range(1, 65):
+        b.step(t)
+    b.check_rows()
+
+
+def test_decode_continuous_batch_ring_offsets():
+    """Sequences of different lengths (different ring offsets, some partly filled),
+    in permuted slots; several steps wrap the ring of the longest."""
+    wl = inputs.Workload("cb", 0, 32, 8, 128, 128, 4, 60, 64, 16, 7, 5, 0, 0, 0, 1 / math.sqrt(128))
+    lengths = [300, 37, 129, 2, 1000]
+    b = Batch(wl, lengths, slots=[3, 0, 6, 1, 4], seed=9, max_batch=8)
+    for t in range(80):
+        b.step(t, isolated=(t % 20 == 0))
+    b.check_rows()
+
+
+def test_decode_subset_of_slots():
+    """Only some sequences of the cache decode in a step; the others do not move."""
+    wl = inputs.Workload("cb", 0, 32, 8, 128, 128, 4, 60, 64, 16, 7, 5, 0, 0, 0, 1 / math.sqrt(128))
+    b = Batch(wl, [300, 200, 150], slots=[0, 1, 2], seed=4)
+    T_before = b.cache.meta()[:, 1].cpu().tolist()
+    sub = torch.tensor([2, 0], dtype=torch.int32, device="cuda")
+    tok = inputs.gen_decode(wl, 2, step=0, seed=1)
+    b.cache.decode_append(sub, tok.k.cuda(), tok.v.cuda())
+    out = b.cache.decode_attn(sub, tok.q.cuda())
+    torch.cuda.synchronize()
+    T_after = b.cache.meta()[:, 1].cpu().tolist()
+    assert T_after == [T_before[0] + 1, T_before[1], T_before[2] + 1]
+    for j, seq in enumerate([2, 0]):
+        oracle.append(b.ocaches[seq], tok.k[j], tok.v[j])
+        check_outputs(out[j], oracle.decode_attn(b.ocaches[seq], tok.q[j]), f"subset {seq}")
+
+
+def test_decode_full_kv_baseline_equals_full_attention():
+    """A cache with L_sink = 0, K = 0 and a ring as long as the whole sequence is the
+    uncompressed baseline: it must equal attention over every token (torch SDPA)."""
+    S, steps = 3000, 5
+    wl = inputs.Workload("full", 0, 32, 8, 128, 128, 0, 0, S + steps, 16, 7, 1, 0, 0, 0,
+                         1 / math.sqrt(128))
+    b = Batch(wl, [S], [0], seed=5)
+    for t in range(steps):
+        out = b.step(t)
+        q = inputs.gen_decode(wl, 1, step=t, seed=b.seed).q[0].float().cuda()
+        k = b.K[0].float().cuda().permute(1, 0, 2).repeat_interleave(4, 0)
+        v = b.V[0].float().cuda().permute(1, 0, 2).repeat_interleave(4, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(q.unsqueeze(1), k, v, scale=wl.sm_scale)
+        assert (out[0].float() - ref.squeeze(1)).abs().max().item() < 2e-2
+
+
+def test_decode_compressed_equals_full_when_cache_covers():
+    """L_sink + K + L_recent >= S with no eviction yet: compressed attention equals
+    attention over the whole prompt."""
+    S = 500
+    wl = inputs.Workload("cover", 0, 32, 8, 128, 128, 4, 100, 512, 16, 7, 1, 0, 0, 0,
+                         1 / math.sqrt(128))
+    b = Batch(wl, [S], [0], seed=6)
+    out = b.step(0, append=False)
+    q = inputs.gen_decode(wl, 1, step=0, seed=b.seed).q[0].float().cuda()
+    k = b.K[0].float().cuda().permute(1, 0, 2).repeat_interleave(4, 0)
+    v = b.V[0].float().cuda().permute(1, 0, 2).repeat_interleave(4, 0)
+    ref = torch.nn.functional.scaled_dot_product_attention(q.unsqueeze(1), k, v, scale=wl.sm_scale)
+    assert (out[0].float() - ref.squeeze(1)).abs().max().item() < 2e-2
+
+
+def test_decode_mla_small():
+    """MLA latent layout: 576-wide keys, values = first 512 columns, 32 query heads."""
+    wl = inputs.Workload("mla_small", 1, 32, 1, 576, 512, 4, 40, 64, 8, 5, 1, 0, 0, 0,
+                         1 / math.sqrt(192))
+    b = Batch(wl, [700, 90], [1, 0], seed=12)
+    for t in range(70):
+        b.step(t, isolated=(t == 69))
+    b.check_rows()
+
+
+def test_decode_out_of_range_slot_reports_without_fault():
+    """A slot index past max_batch is rejected by the kernels through the status word
+    (the call itself returns OK: the index lives on the device)."""
+    wl = inputs.Workload("cb", 0, 32, 8, 128, 128, 4, 60, 64, 16, 7, 1, 0, 0, 0, 1 / math.sqrt(128))
+    b = Batch(wl, [100], [0], seed=1, max_batch=2)
+    bad = torch.tensor([5], dtype=torch.int32, device="cuda")
+    tok = inputs.gen_decode(wl, 1, step=0, seed=1)
+    b.cache.decode_append(bad, tok.k.cuda(), tok.v.cuda())
+    assert b.cache.check_device() == snap.SNAP_ERR_DEVICE_CHECK
+    out = b.cache.decode_attn(bad, tok.q.cuda())
+    assert b.cache.check_device() == snap.SNAP_ERR_DEVICE_CHECK
+    assert float(out.float().abs().sum()) == 0.0
+    assert b.cache.check_device() == snap.SNAP_OK  # cleared by the previous read
