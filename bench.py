@@ -148,7 +148,7 @@ def algorithmic_decode_bytes(wl, metas):
         S, T, R0, n_sink, n_mid = m
         valid += n_sink + n_mid + min(T - R0, wl.L_recent)
     n = len(metas)
-    return valid * row + n * wl.n_q_heads * (wl.d_qk + wl.d_v) * 2
+    return valid * row + n * wl.n_q_heads * (wl.d_qk * 2 + wl.d_v * 4)
 
 
 def run_ours(args):
@@ -177,7 +177,7 @@ def run_ours(args):
     cfg = snap.make_config(**wl.config_kwargs())
     cache = snap.SnapCache(cfg, max_batch=B, max_prompt=max(lengths), max_n=B, device=dev, stream=stream)
     slots = torch.arange(B, dtype=torch.int32, device=dev)
-    out = torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev)
     split_count = None
 
     def barrier():
@@ -384,18 +384,18 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
     hQ = [p.Q.to("cpu").pin_memory() for p in pre]
     hq, hk = q_all.to("cpu").pin_memory(), k_all.to("cpu").pin_memory()
     hv = v_all.to("cpu").pin_memory() if v_all is not None else None
-    hout = torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.bfloat16).pin_memory()
+    hout = torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.float32).pin_memory()
     dK = [torch.empty_like(p.K) for p in pre]
     dV = [torch.empty_like(p.V) if p.V is not None else None for p in pre]
     dQ = [torch.empty_like(p.Q) for p in pre]
     dq, dk = torch.empty_like(q_all[0]), torch.empty_like(k_all[0])
     dv = torch.empty_like(v_all[0]) if v_all is not None else None
-    dout = torch.empty((B, wl.n_q_heads, wl.d_v), dtype=torch.bfloat16, device=dev)
+    dout = torch.empty((B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev)
     cache = snap.SnapCache(cfg, max_batch=B, max_prompt=max(lengths), max_n=B, device=dev, stream=stream)
     slots = torch.arange(B, dtype=torch.int32, device=dev)
     h2d = sum(x.numel() * 2 for x in hK + hQ) + sum(x.numel() * 2 for x in hV if x is not None)
     h2d += D * (dq.numel() + dk.numel() + (dv.numel() if dv is not None else 0)) * 2
-    d2h = D * dout.numel() * 2
+    d2h = D * dout.numel() * 4
 
     def step():
         with torch.cuda.stream(stream):

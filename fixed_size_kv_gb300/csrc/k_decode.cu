@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
             report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
         if (a.splits == 1)  // otherwise the merge kernel writes the zeros
             for (int i = threadIdx.x; i < c.G * GD; i += blockDim.x)
-                a.out[((size_t)b * c.Hq + (size_t)h * c.G) * GD + i] = __float2bfloat16_rn(0.f);
+                a.out[((size_t)b * c.Hq + (size_t)h * c.G) * GD + i] = 0.f;
         return;
     }
     const snap_seq_meta m = a.meta[slot];
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
         }
         if (a.splits == 1) {
             const float r = L > 0.f ? O / L : 0.f;
-            a.out[((size_t)b * c.Hq + (size_t)h * c.G + hh) * GD + d] = __float2bfloat16_rn(r);
+            a.out[((size_t)b * c.Hq + (size_t)h * c.G + hh) * GD + d] = r;
         } else {
             const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + split) * c.G + hh;
             a.part_o[pi * GD + d] = O;
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a) {
         if (tid == 0 && split == 0 && hb == 0) report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
         if (a.splits == 1)
             for (int i = tid; i < MLA_HB * MV; i += blockDim.x)
-                a.out[((size_t)b * c.Hq + (size_t)hb * MLA_HB) * MV + i] = __float2bfloat16_rn(0.f);
+                a.out[((size_t)b * c.Hq + (size_t)hb * MLA_HB) * MV + i] = 0.f;
         return;
     }
     const snap_seq_meta m = a.meta[slot];
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a) {
             if (a.splits == 1) {
                 const float L = l_s[row];
                 const float r = L > 0.f ? o[nt][i] / L : 0.f;
-                a.out[((size_t)b * c.Hq + head) * MV + d] = __float2bfloat16_rn(r);
+                a.out[((size_t)b * c.Hq + head) * MV + d] = r;
             } else {
                 const size_t pi = ((size_t)b * a.splits + split) * c.Hq + head;
                 a.part_o[pi * MV + d] = o[nt][i];
@@ -494,7 +494,7 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
                 const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + s) * c.G + hh;
                 O += ex2(a.part_ml[pi * 2] - M) * a.part_o[pi * c.dv + d];
             }
-        a.out[((size_t)b * c.Hq + i) * c.dv + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+        a.out[((size_t)b * c.Hq + i) * c.dv + d] = L > 0.f ? O / L : 0.f;
     }
 }
 

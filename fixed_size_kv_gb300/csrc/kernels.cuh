@@ -15,7 +15,7 @@ struct DecodeArgs {
     const int32_t* slots;        // [n]
     int n;
     const bf16* q;               // [n][Hq][dqk]
-    bf16* out;                   // [n][Hq][dv]
+    float* out;                  // [n][Hq][dv] fp32
     float* part_o;               // [n][Hkv][splits][G][dv]
     float* part_ml;              // [n][Hkv][splits][G][2]  (max, sum) base-2 domain
     int splits;

@@ -217,8 +217,9 @@ class SnapCache:
         assert slots.dtype == torch.int32 and slots.is_contiguous()
         n = slots.numel()
         if out is None:
-            out = torch.empty((n, self.cfg.n_q_heads, self.cfg.d_v), dtype=torch.bfloat16,
+            out = torch.empty((n, self.cfg.n_q_heads, self.cfg.d_v), dtype=torch.float32,
                               device=self.device)
+        assert out.dtype == torch.float32 and out.is_contiguous()
         _check(load().snap_decode_attn(self.handle, _ptr(slots), n, _ptr(q.contiguous()), _ptr(out),
                                        _ptr(self.ws_decode), self.ws_decode.numel(), _stream(stream)),
                "snap_decode_attn")

@@ -176,7 +176,8 @@ snap_status snap_decode_attn_ws_bytes(const snap_config* cfg, int max_n, size_t*
  * ring slots holding positions max(R0, T - L_recent) .. T-1) of sm_scale * q.k,
  * weighted sum of the values.  The query attends to what the cache holds now: call
  * snap_decode_append() first to include the current token.
- *  q     bf16 [n][n_q_heads][d_qk];  out bf16 [n][n_q_heads][d_v]
+ *  q     bf16 [n][n_q_heads][d_qk];  out fp32 [n][n_q_heads][d_v] (the fp32 accumulation,
+ *        not rounded to bf16)
  *  ws    device workspace of snap_decode_attn_ws_bytes(cfg, n) bytes
  * A full (uncompressed) KV cache is the same call on a cache configured with
  * L_sink = 0, K = 0, L_recent = maximum length.
