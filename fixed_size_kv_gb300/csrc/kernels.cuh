@@ -1,6 +1,8 @@
 // kernels.cuh -- launch interfaces between the C-ABI layer and the kernels.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace snap {
@@ -59,10 +61,11 @@ struct CompressArgs {
     int slot;
     // workspace
     float* part_ml;              // [Hkv][R][row_splits][2]
-    float* lse2;                 // [Hkv][R]
-    float* col;                  // [Hkv][S_pad]
+    float* nlse2;                // [Hkv][R_pad]  -lse2 per observation row (-inf padding)
+    float* col;                  // [2][Hkv][S_pad] column-sum halves (summed by select)
     uint32_t* pool;              // [Hkv][S_pad] pooled score bits
-    int row_splits;
+    int row_splits;              // partials per row (2 per key split)
+    int R_pad;
     int64_t S_pad;
     // cache
     bf16* kc;
@@ -73,13 +76,27 @@ struct CompressArgs {
     DevConfig cfg;
 };
 
-constexpr int CMP_KEYS = 64;     // keys per tile in the score passes
-constexpr int CMP_ROWS = 64;     // observation rows per tile in the score passes
-
-cudaError_t launch_rowstat(const CompressArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_lse_merge(const CompressArgs& a, cudaStream_t st);
-cudaError_t launch_colsum(const CompressArgs& a, int num_sms, cudaStream_t st);
 cudaError_t launch_select(const CompressArgs& a, cudaStream_t st);
+
+// ------------------------------------------------- score GEMM (tcgen05 + TMA)
+struct ScoreParams {
+    int S, W, R, G, Hkv;
+    float sl2;                   // sm_scale * log2(e)
+    int n_sc;                    // S - W scored prefix positions
+    int n_units, splits, x_tiles;
+    int Ny;                      // rows of the Y operand per MMA (N), multiple of 64, <= 256
+    int R_pad;
+    float* part_ml;              // ROWSTAT out: [Hkv][R][2*splits][2]
+    const float* nlse2;          // COLSUM in:  [Hkv][R_pad]
+    float* col;                  // COLSUM out: [2][Hkv][S_pad]
+    int64_t S_pad;
+    float* logits;               // LOGITS out: [Hkv][R][S]
+    int32_t* status;
+};
+enum { SCORE_ROWSTAT = 0, SCORE_COLSUM = 1, SCORE_LOGITS = 2 };
+cudaError_t launch_score_tc(int mode, const CUtensorMap& tx, const CUtensorMap& ty, const ScoreParams& p,
+                            int D, bool x_is_q, bool x_resident, int num_sms, cudaStream_t st);
 cudaError_t launch_cache_write(const CompressArgs& a, int num_sms, cudaStream_t st);
 
 }  // namespace snap

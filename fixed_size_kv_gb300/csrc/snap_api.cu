@@ -1,5 +1,7 @@
 // snap_api.cu -- the C ABI of libsnap (see include/snap.h): argument checks,
 // cache/workspace layout, and the launch sequence of each entry point.
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -24,7 +26,7 @@ struct snap_cache {
 namespace {
 
 constexpr int ABI_VERSION = 1;
-constexpr int MAX_ROW_SPLITS = 64;
+constexpr int MAX_KEY_SPLITS = 32;   // key splits of the row pass (2 partials each)
 constexpr int MAX_DECODE_SPLITS = 32;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -88,26 +90,116 @@ CacheRegions regions(const snap_config& c, int max_batch) {
 
 // Compress workspace regions for a prompt of S tokens.
 struct CompressWs {
-    size_t part_ml, lse2, col, pool, total;
+    size_t part_ml, nlse2, col, pool, total;
     int64_t S_pad;
+    int R, R_pad;
 };
 
 CompressWs compress_ws(const snap_config& c, int64_t S) {
     const int G = c.n_q_heads / c.n_kv_heads;
-    const size_t R = (size_t)G * c.W;
     CompressWs w;
-    w.S_pad = (S + 63) / 64 * 64;
+    w.R = G * c.W;
+    w.R_pad = (w.R + 255) / 256 * 256;
+    w.S_pad = (S + 127) / 128 * 128;
     size_t off = 0;
     w.part_ml = off;
-    off = align_up(off + sizeof(float) * 2 * c.n_kv_heads * R * MAX_ROW_SPLITS, 256);
-    w.lse2 = off;
-    off = align_up(off + sizeof(float) * c.n_kv_heads * R, 256);
+    off = align_up(off + sizeof(float) * 2 * c.n_kv_heads * (size_t)w.R * 2 * MAX_KEY_SPLITS, 256);
+    w.nlse2 = off;
+    off = align_up(off + sizeof(float) * c.n_kv_heads * (size_t)w.R_pad, 256);
     w.col = off;
-    off = align_up(off + sizeof(float) * c.n_kv_heads * (size_t)w.S_pad, 256);
+    off = align_up(off + sizeof(float) * 2 * c.n_kv_heads * (size_t)w.S_pad, 256);
     w.pool = off;
     off = align_up(off + sizeof(uint32_t) * c.n_kv_heads * (size_t)w.S_pad, 256);
     w.total = off;
     return w;
+}
+
+// ------------------------------------------------------------ TMA tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+            const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Observation queries [W][Hq][d] of KV head h as rows (w, g): dims {d, G, W, Hkv}.
+bool q_map(CUtensorMap* m, const void* Q, const snap_config& c, int box_rows) {
+    const int G = c.n_q_heads / c.n_kv_heads;
+    const cuuint64_t dims[4] = {(cuuint64_t)c.d_qk, (cuuint64_t)G, (cuuint64_t)c.W, (cuuint64_t)c.n_kv_heads};
+    const cuuint64_t strides[3] = {(cuuint64_t)c.d_qk * 2, (cuuint64_t)c.n_q_heads * c.d_qk * 2,
+                                   (cuuint64_t)G * c.d_qk * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)G, (cuuint32_t)(box_rows / G), 1};
+    return encode(m, Q, 4, dims, strides, box);
+}
+
+// Prompt keys (strided): dims {d, S, Hkv}.
+bool k_map(CUtensorMap* m, const void* K, int64_t S, const snap_config& c, int64_t tok_stride,
+           int64_t head_stride, int box_rows) {
+    const cuuint64_t dims[3] = {(cuuint64_t)c.d_qk, (cuuint64_t)S, (cuuint64_t)c.n_kv_heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)tok_stride * 2,
+                                   (cuuint64_t)(head_stride > 0 ? head_stride : c.d_qk) * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    return encode(m, K, 3, dims, strides, box);
+}
+
+ScoreParams score_params(const snap_config& c, int64_t S, const CompressWs& w, uint8_t* ws, int32_t* status) {
+    ScoreParams sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.S = (int)S;
+    sp.W = c.W;
+    sp.R = w.R;
+    sp.G = c.n_q_heads / c.n_kv_heads;
+    sp.Hkv = c.n_kv_heads;
+    sp.sl2 = c.sm_scale * 1.4426950408889634f;
+    sp.n_sc = (int)S - c.W;
+    sp.R_pad = w.R_pad;
+    sp.S_pad = w.S_pad;
+    if (ws) {
+        sp.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
+        sp.nlse2 = reinterpret_cast<const float*>(ws + w.nlse2);
+        sp.col = reinterpret_cast<float*>(ws + w.col);
+    }
+    sp.status = status;
+    return sp;
+}
+
+// Key splits of the row pass: about two units per SM.
+int row_key_splits(const snap_config& c, int R, int64_t S) {
+    const int per = c.n_kv_heads * ((R + 127) / 128);
+    const int ny = (int)((S + 255) / 256);
+    int splits = (2 * num_sms() + per - 1) / per;
+    if (splits > MAX_KEY_SPLITS) splits = MAX_KEY_SPLITS;
+    if (splits > ny) splits = ny;
+    if (splits < 1) splits = 1;
+    return splits;
+}
+
+// Row pass: X = 128 observation rows, Y = 256-key tiles.
+cudaError_t run_rowstat(int mode, const snap_config& c, ScoreParams sp, const void* K, int64_t S,
+                        int64_t tok_stride, int64_t head_stride, const void* Q, cudaStream_t st) {
+    CUtensorMap tx, ty;
+    if (!q_map(&tx, Q, c, 128) || !k_map(&ty, K, S, c, tok_stride, head_stride, 256)) return cudaErrorInvalidValue;
+    sp.Ny = 256;
+    sp.x_tiles = (sp.R + 127) / 128;
+    sp.splits = row_key_splits(c, sp.R, S);
+    sp.n_units = c.n_kv_heads * sp.x_tiles * sp.splits;
+    return launch_score_tc(mode, tx, ty, sp, c.d_qk, true, true, num_sms(), st);
 }
 
 size_t decode_ws_bytes(const snap_config& c, int max_n) {
@@ -132,6 +224,8 @@ snap_status check_config(const snap_config* c) {
         if (c->d_qk != 128 || c->d_v != 128) return SNAP_ERR_UNSUPPORTED;
         if (c->n_q_heads / c->n_kv_heads > 8) return SNAP_ERR_UNSUPPORTED;
     }
+    // observation rows are loaded as whole query-head groups by the score GEMM
+    if (128 % (c->n_q_heads / c->n_kv_heads)) return SNAP_ERR_UNSUPPORTED;
     return SNAP_OK;
 }
 
@@ -292,26 +386,61 @@ snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void
         if (reinterpret_cast<uintptr_t>(ws) & 255u) return SNAP_ERR_INVALID_ARG;
         uint8_t* wb = static_cast<uint8_t*>(ws);
         a.part_ml = reinterpret_cast<float*>(wb + w.part_ml);
-        a.lse2 = reinterpret_cast<float*>(wb + w.lse2);
+        a.nlse2 = reinterpret_cast<float*>(wb + w.nlse2);
         a.col = reinterpret_cast<float*>(wb + w.col);
         a.pool = reinterpret_cast<uint32_t*>(wb + w.pool);
         a.S_pad = w.S_pad;
-        // row splits: about two waves of rowstat CTAs
-        const int row_blocks = (a.R + CMP_ROWS - 1) / CMP_ROWS;
-        const int per_sm = c.d_qk == 128 ? 4 : 1;
-        const int nkt = (int)((S + CMP_KEYS - 1) / CMP_KEYS);
-        int rs = (2 * num_sms() * per_sm + row_blocks * c.n_kv_heads - 1) / (row_blocks * c.n_kv_heads);
-        if (rs > MAX_ROW_SPLITS) rs = MAX_ROW_SPLITS;
-        if (rs > nkt) rs = nkt;
-        if (rs < 1) rs = 1;
-        a.row_splits = rs;
-        cudaError_t e = launch_rowstat(a, num_sms(), st);
-        if (e == cudaSuccess) e = launch_lse_merge(a, st);
-        if (e == cudaSuccess) e = launch_colsum(a, num_sms(), st);
+        a.R_pad = w.R_pad;
+        ScoreParams sp = score_params(c, S, w, wb, cache->status);
+        // 1. row pass: partial log-sum-exp of every observation row
+        cudaError_t e = run_rowstat(SCORE_ROWSTAT, c, sp, K, S, tok_stride, head_stride, Q_obs, st);
+        // 2. merge into -lse2 per row
+        if (e == cudaSuccess) {
+            a.row_splits = 2 * row_key_splits(c, w.R, S);
+            e = launch_lse_merge(a, st);
+        }
+        // 3. column pass: X = 128-key tiles, Y = observation rows
+        if (e == cudaSuccess) {
+            CUtensorMap tx, ty;
+            const int nx = (int)((S - c.W + 127) / 128);
+            const int ny64 = (w.R + 63) / 64 * 64;
+            const bool y_resident = c.d_qk == 128 && ny64 <= 256;
+            sp.Ny = y_resident ? ny64 : 256;
+            if (!k_map(&tx, K, S, c, tok_stride, head_stride, 128) || !q_map(&ty, Q_obs, c, sp.Ny))
+                return SNAP_ERR_INVALID_ARG;
+            if (y_resident) {
+                int splits = (num_sms() + c.n_kv_heads - 1) / c.n_kv_heads;
+                if (splits > nx) splits = nx;
+                if (splits < 1) splits = 1;
+                sp.splits = splits;
+                sp.n_units = c.n_kv_heads * splits;
+            } else {
+                sp.splits = 1;
+                sp.n_units = c.n_kv_heads * nx;
+            }
+            e = launch_score_tc(SCORE_COLSUM, tx, ty, sp, c.d_qk, false, !y_resident, num_sms(), st);
+        }
+        // 4. pool + top-K
         if (e == cudaSuccess) e = launch_select(a, st);
         if (e != cudaSuccess) return cuda_status(e);
     }
     return cuda_status(launch_cache_write(a, num_sms(), st));
+}
+
+snap_status snap_window_logits(snap_cache* cache, const void* K, int64_t S, int64_t tok_stride,
+                               int64_t head_stride, const void* Q_obs, float* out, void* stream) {
+    if (!cache || !K || !Q_obs || !out) return SNAP_ERR_INVALID_ARG;
+    const snap_config& c = cache->cfg;
+    if (S < c.W || S > (1ll << 30)) return SNAP_ERR_SHAPE;
+    if (!aligned16(K) || !aligned16(Q_obs) || !aligned16(out)) return SNAP_ERR_INVALID_ARG;
+    if (tok_stride < c.d_qk || (tok_stride * 2) % 16 || head_stride < 0 || (head_stride * 2) % 16)
+        return SNAP_ERR_INVALID_ARG;
+    if (c.n_kv_heads > 1 && head_stride < c.d_qk) return SNAP_ERR_INVALID_ARG;
+    const CompressWs w = compress_ws(c, S);
+    ScoreParams sp = score_params(c, S, w, nullptr, cache->status);
+    sp.logits = out;
+    return cuda_status(run_rowstat(SCORE_LOGITS, c, sp, K, S, tok_stride, head_stride, Q_obs,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 snap_status snap_decode_append(snap_cache* cache, const int32_t* slots, int n, const void* k_new,
@@ -359,7 +488,7 @@ snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, con
     a.slots = slots;
     a.n = n;
     a.q = static_cast<const bf16*>(q);
-    a.out = static_cast<bf16*>(out);
+    a.out = static_cast<float*>(out);
     a.status = cache->status;
     a.cfg = dev_config(c, cache->max_batch);
     const int key_tile = c.layout == SNAP_LAYOUT_GQA ? GQA_KEYS : MLA_KEYS;

@@ -58,6 +58,7 @@ SIGNATURES = {
     "snap_cache_view_get": (_I, [_VP, _P(snap_cache_view)]),
     "snap_compress_ws_bytes": (_I, [_P(snap_config), _I64, _P(_SZ)]),
     "snap_compress": (_I, [_VP, _I, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
+    "snap_window_logits": (_I, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP]),
     "snap_decode_append": (_I, [_VP, _VP, _I, _VP, _VP, _VP]),
     "snap_decode_attn_ws_bytes": (_I, [_P(snap_config), _I, _P(_SZ)]),
     "snap_decode_attn": (_I, [_VP, _VP, _I, _VP, _VP, _VP, _SZ, _VP]),
@@ -204,6 +205,17 @@ class SnapCache:
         _check(load().snap_compress(self.handle, slot, _ptr(K), _ptr(V), S, K.stride(0), K.stride(1),
                                     _ptr(Q_obs), _ptr(self.ws_compress), self.ws_compress.numel(),
                                     _stream(stream)), "snap_compress")
+
+    def window_logits(self, K: torch.Tensor, Q_obs: torch.Tensor, stream=None) -> torch.Tensor:
+        """Base-2 logits of the observation rows against every prompt key:
+        fp32 [H_kv][G*W][S] (the compression's score GEMM, for inspection)."""
+        S = K.shape[0]
+        G = self.cfg.n_q_heads // self.cfg.n_kv_heads
+        out = torch.empty((self.cfg.n_kv_heads, G * self.cfg.W, S), dtype=torch.float32, device=self.device)
+        Q_obs = Q_obs.contiguous()
+        _check(load().snap_window_logits(self.handle, _ptr(K), S, K.stride(0), K.stride(1), _ptr(Q_obs),
+                                         _ptr(out), _stream(stream)), "snap_window_logits")
+        return out
 
     def decode_append(self, slots: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor | None,
                       stream=None) -> None:

@@ -157,6 +157,17 @@ snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void
                           void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Inspection of the compression's score GEMM: the base-2 logits
+ * out[h][r][j] = log2(e) * sm_scale * q_r . k_j  (fp32 [n_kv_heads][G*W][S]) of every
+ * observation row r = w*G + g (query head h*G+g at position S-W+w) against every
+ * prompt key j, computed by the same tensor-core kernel that scores prompts in
+ * snap_compress().  Arguments as for snap_compress(); S >= W.  Uses the cache handle
+ * for its configuration and status word only.
+ */
+snap_status snap_window_logits(snap_cache* cache, const void* K, int64_t S, int64_t tok_stride,
+                               int64_t head_stride, const void* Q_obs, float* out, void* stream);
+
+/*
  * Decode-step append for a continuous batch ("Ring Buffer vs. Naive Slicing"): for each
  * b < n, the new token of sequence slots[b] (position T) is written into ring slot
  * L_sink + K + (T mod L_recent), then T += 1.  No gather, no concat.
