@@ -4,6 +4,7 @@
 
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "kernels.cuh"
@@ -530,3 +531,86 @@ snap_status snap_check_device(snap_cache* cache, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode attention without a caller workspace (snap_decode_attn_noalloc).
+//
+// The split-KV partial results live in this file-scope device array instead of a
+// caller-allocated workspace.  Host code cannot use the array's name as a device
+// address: the device address is looked up once per device with
+// cudaGetSymbolAddress and then passed to the kernels as an ordinary pointer.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SNAP_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of the scratch array on the current device (looked up on first use).
+snap_status noalloc_scratch(void** out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return SNAP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_status(e);
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return SNAP_OK;
+}
+
+}  // namespace
+
+extern "C" snap_status snap_decode_attn_noalloc(snap_cache* cache, const int32_t* slots, int n, const void* q,
+                                                void* out, void* stream) {
+    if (!cache || n < 0) return SNAP_ERR_INVALID_ARG;
+    if (n == 0) return SNAP_OK;
+    if (!slots || !q || !out || !aligned16(q) || !aligned16(out)) return SNAP_ERR_INVALID_ARG;
+    if (n > cache->max_batch) return SNAP_ERR_INVALID_ARG;
+    const snap_config& c = cache->cfg;
+    DecodeArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.kc = cache->k;
+    a.vc = cache->v;
+    a.meta = cache->meta;
+    a.slots = slots;
+    a.n = n;
+    a.q = static_cast<const bf16*>(q);
+    a.out = static_cast<float*>(out);
+    a.status = cache->status;
+    a.cfg = dev_config(c, cache->max_batch);
+    const int key_tile = c.layout == SNAP_LAYOUT_GQA ? GQA_KEYS : MLA_KEYS;
+    const int tiles = (int)((cache->C + key_tile - 1) / key_tile);
+    const int base = c.layout == SNAP_LAYOUT_GQA ? n * c.n_kv_heads : n * (c.n_q_heads / MLA_HB);
+    const int splits = decode_splits(base, c.layout == SNAP_LAYOUT_GQA ? tiles / 4 : tiles, 1);
+    a.splits = splits;
+    a.tiles_per_split = (tiles + splits - 1) / splits;
+    if (splits > 1) {
+        // compact partial layout for this call: O then (max, sum)
+        const size_t parts = (size_t)n * c.n_q_heads * splits;
+        const size_t o_bytes = align_up(parts * sizeof(float) * c.d_v, 256);
+        const size_t need = o_bytes + parts * sizeof(float) * 2;
+        if (need > SNAP_NOALLOC_SCRATCH_BYTES) {
+            std::fprintf(stderr,
+                         "libsnap: snap_decode_attn_noalloc needs %zu bytes of scratch for %d sequences; the "
+                         "limit is %u (use snap_decode_attn with a workspace)\n",
+                         need, n, SNAP_NOALLOC_SCRATCH_BYTES);
+            return SNAP_ERR_SHAPE;
+        }
+        void* scratch = nullptr;
+        const snap_status s = noalloc_scratch(&scratch);
+        if (s != SNAP_OK) return s;
+        a.part_o = static_cast<float*>(scratch);
+        a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + o_bytes);
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = c.layout == SNAP_LAYOUT_GQA ? launch_decode_gqa(a, st) : launch_decode_mla(a, st);
+    if (e == cudaSuccess && splits > 1) e = launch_decode_merge(a, st);
+    return cuda_status(e);
+}

@@ -63,6 +63,7 @@ SIGNATURES = {
     "snap_decode_attn_ws_bytes": (_I, [_P(snap_config), _I, _P(_SZ)]),
     "snap_decode_attn": (_I, [_VP, _VP, _I, _VP, _VP, _VP, _SZ, _VP]),
     "snap_check_device": (_I, [_VP, _VP]),
+    "snap_decode_attn_noalloc": (_I, [_VP, _VP, _I, _VP, _VP, _VP]),
 }
 
 _lib = None
@@ -236,6 +237,15 @@ class SnapCache:
                                        _ptr(self.ws_decode), self.ws_decode.numel(), _stream(stream)),
                "snap_decode_attn")
         return out
+
+    def decode_attn_noalloc(self, slots: torch.Tensor, q: torch.Tensor, out: torch.Tensor,
+                            stream=None) -> int:
+        """snap_decode_attn_noalloc: the same attention with the split partials in the
+        library's fixed scratch array (no workspace).  Returns the status code."""
+        assert slots.dtype == torch.int32 and slots.is_contiguous()
+        assert out.dtype == torch.float32 and out.is_contiguous()
+        return load().snap_decode_attn_noalloc(self.handle, _ptr(slots), slots.numel(), _ptr(q.contiguous()),
+                                               _ptr(out), _stream(stream))
 
     def check_device(self, stream=None) -> int:
         return load().snap_check_device(self.handle, _stream(stream))

@@ -202,6 +202,43 @@ snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, con
  */
 snap_status snap_check_device(snap_cache* cache, void* stream);
 
+/*
+ * Bytes of device scratch that snap_decode_attn_noalloc() draws on (32 MiB).  The
+ * array is part of the library's device image: every GPU that loads libsnap holds
+ * it until the process exits.
+ */
+#define SNAP_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * snap_decode_attn() for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this is a packaging variant of the same decode attention.
+ *
+ * Who needs it: code that runs where cudaMalloc is unavailable or unwelcome, for
+ * example inside a host callback, a signal-safe or real-time thread, a stream
+ * being captured into a CUDA graph, or an embedding runtime that owns every device
+ * allocation itself.  Such a caller cannot obtain the workspace snap_decode_attn()
+ * needs for its split-KV partial results.  This entry point takes the same inputs
+ * and output (q, out, slots; the cache it attends over) and keeps the partial results
+ * in a fixed scratch array compiled into the library instead.  It never calls
+ * cudaMalloc, cudaFree or any allocating routine.
+ *
+ *  - Limit: the partial results of one call (n * n_q_heads * splits * (d_v + 2) floats,
+ *    splits chosen as in snap_decode_attn) must fit SNAP_NOALLOC_SCRATCH_BYTES; larger
+ *    batches are rejected with SNAP_ERR_SHAPE (and a line on stderr) before anything is
+ *    launched.  Examples that fit: 16 sequences of 32 x 128 GQA heads; 64 sequences of
+ *    the same shape with a 8192-slot cache; up to 6 sequences of the 128-head MLA shape
+ *    with a 32768-slot cache.
+ *  - Set-up: the first call on each device looks up the scratch array's device address
+ *    (a host-side query, no allocation) with that device current.  Make that first call
+ *    before capturing a stream into a graph.
+ *  - Sharing: every call on a device uses the same array, and it keeps the previous
+ *    call's contents.  Each call overwrites every partial it reads, so nothing needs
+ *    clearing, but calls that overlap on the GPU (different streams without ordering,
+ *    or concurrent graphs) race on the scratch: order them.
+ */
+snap_status snap_decode_attn_noalloc(snap_cache* cache, const int32_t* slots, int n, const void* q,
+                                     void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
