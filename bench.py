@@ -514,10 +514,121 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_mixed(args):
+    """Continuous batch with arrivals (the 64-slot mixed workload): every
+    `arrival_every` decode steps, the slots whose request finished take new requests,
+    which are compressed on a second stream while the first keeps decoding the
+    others; a new request joins the decode batch at the next arrival boundary.
+    value = decoded tokens / wall time of the whole run (compressions included)."""
+    import torch
+    from fixed_size_kv_gb300 import inputs, snap
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    snap.load(build_if_missing=True)
+    wl = inputs.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.replace(batch=args.batch)
+    B, D, every = wl.batch, wl.decode_steps, wl.arrival_every
+    sa, sb = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    n_req = B * 16
+    lengths = inputs.prompt_lengths(wl, args.seed, n=n_req)
+    outs = inputs.output_lengths(args.seed, n_req)
+    # a pool of prompt buffers at the longest length; request i reads a prefix of pool[i % NP]
+    NP = 8
+    with torch.cuda.stream(sa):
+        pool = [inputs.gen_prefill(wl, wl.prompt_max, seed=args.seed, seq=i, device=dev) for i in range(NP)]
+        toks = [inputs.gen_decode(wl, B, step=t, seed=args.seed, device=dev) for t in range(64)]
+    sa.synchronize()
+    cfg = snap.make_config(**wl.config_kwargs())
+    cache = snap.SnapCache(cfg, max_batch=B, max_prompt=wl.prompt_max, max_n=B, device=dev, stream=sa)
+    out = torch.empty((B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev)
+
+    def compress(slot, req, stream):
+        p = pool[req % NP]
+        S = lengths[req]
+        cache.compress(slot, p.K[:S], p.V[:S] if p.V is not None else None, p.Q, stream=stream)
+
+    def run(steps, timed):
+        next_req = 0
+        remaining = [0] * B
+        for slot in range(B):                    # initial fill, before the clock starts
+            compress(slot, next_req, sa)
+            remaining[slot] = outs[next_req]
+            next_req += 1
+        sa.synchronize()
+        pending = {}                             # slot -> remaining, joining at the next boundary
+        ev_b = None
+        tokens = 0
+        n_compress = 0
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(sa)
+        active = [s for s in range(B) if remaining[s] > 0]
+        slots_t = torch.tensor(active, dtype=torch.int32).to(dev, non_blocking=True)
+        for t in range(steps):
+            if t > 0 and t % every == 0:
+                if pending:
+                    sa.wait_event(ev_b)
+                    for s, r in pending.items():
+                        remaining[s] = r
+                    pending = {}
+                free = [s for s in range(B) if remaining[s] == 0]
+                if free:
+                    for s in free:
+                        compress(s, next_req % n_req, sb)
+                        pending[s] = outs[next_req % n_req]
+                        next_req += 1
+                        n_compress += 1
+                    ev_b = torch.cuda.Event()
+                    ev_b.record(sb)
+                active = [s for s in range(B) if remaining[s] > 0]
+                with torch.cuda.stream(sa):
+                    slots_t = torch.tensor(active, dtype=torch.int32).to(dev, non_blocking=True)
+            n = len(active)
+            if n:
+                tk = toks[t % 64]
+                cache.decode_append(slots_t, tk.k[:n], tk.v[:n] if tk.v is not None else None, stream=sa)
+                cache.decode_attn(slots_t, tk.q[:n], out=out[:n], stream=sa)
+                tokens += n
+                done = False
+                for s in active:
+                    remaining[s] -= 1
+                    done |= remaining[s] == 0
+                if done:
+                    active = [s for s in active if remaining[s] > 0]
+                    with torch.cuda.stream(sa):
+                        slots_t = torch.tensor(active, dtype=torch.int32).to(dev, non_blocking=True)
+        e1.record(sa)
+        torch.cuda.synchronize(dev)
+        return tokens, e0.elapsed_time(e1), n_compress
+
+    run(min(D, 64), False)                       # warm-up
+    clocks = ClockSampler(0)
+    clocks.start()
+    tokens, ms, n_compress = run(D, True)
+    clk = clocks.stop()
+    st = cache.check_device(sa)
+    if st != snap.SNAP_OK:
+        raise RuntimeError(f"device status: {snap.status_string(st)}")
+    line = {"metric": METRIC, "value": tokens / (ms / 1e3), "unit": "tok/s", "n_gpus": 1, "steps": D,
+            "warmup": 1, "ms_per_step": ms / D, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "slots": B, "prompt_len": f"U[{wl.prompt_min},{wl.prompt_max}]",
+                       "decode_steps": D, "arrival_every": every,
+                       "cache": f"{wl.L_sink}+{wl.K}+{wl.L_recent}={wl.C}",
+                       "output_len": "U[32,1024]", "prompt_pool": NP},
+            "decoded_tokens": tokens, "arrivals_compressed": n_compress, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    from fixed_size_kv_gb300 import inputs
+    if inputs.WORKLOADS[args.workload].arrival_every > 0:
+        run_mixed(args)
     else:
         run_ours(args)
 
