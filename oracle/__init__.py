@@ -60,11 +60,21 @@ class _Meta(ctypes.Structure):
                 ("R0", ctypes.c_int64), ("n_mid", ctypes.c_int64)]
 
 
+def build_mutant(k: int, out_dir: str) -> str:
+    """Builds the oracle with deliberate mistake number k (tests of the pins only)."""
+    src = os.path.join(_HERE, "snap_oracle.c")
+    path = os.path.join(out_dir, f"liboracle_mutant{k}.so")
+    subprocess.check_call(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                           f"-DORACLE_MUTANT={k}", "-o", path, src, "-lm"])
+    return path
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # SNAP_ORACLE_LIB points the pins at a deliberately broken build (mutation tests)
+            lib = ctypes.CDLL(os.environ.get("SNAP_ORACLE_LIB") or build())
             P = ctypes.POINTER
             i64, vp = ctypes.c_int64, ctypes.c_void_p
             lib.snap_oracle_check_config.argtypes = [P(_Config)]

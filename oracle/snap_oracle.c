@@ -20,6 +20,12 @@
 #include <stdlib.h>
 #include <string.h>
 
+/* ORACLE_MUTANT selects one deliberately wrong variant (tests only: it shows that the
+ * pins in tests/test_oracle_pins.py catch plausible mistakes).  0 = the oracle. */
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
 static double bf16_value(uint16_t b)
 {
     uint32_t u = ((uint32_t)b) << 16;
@@ -89,14 +95,16 @@ int snap_oracle_window_scores(const snap_oracle_config* c, int64_t S,
         for (int w = 0; w < c->W; ++w) {
             const int64_t pos = S - c->W + w; /* absolute position of this query */
             for (int g = 0; g < G; ++g) {
-                const uint16_t* q = Q + ((int64_t)w * c->n_q_heads + (int64_t)h * G + g) * d;
+                const uint16_t* q = Q + ((int64_t)w * c->n_q_heads +
+                                         (ORACLE_MUTANT == 3 ? (int64_t)g * c->n_kv_heads + h
+                                                             : (int64_t)h * G + g)) * d;
                 /* causal row: keys 0..pos */
                 double mx = -INFINITY;
-                for (int64_t j = 0; j <= pos; ++j) {
+                for (int64_t j = 0; j <= pos - (ORACLE_MUTANT == 2); ++j) {
                     const uint16_t* k = Kp + j * k_tok_stride + (int64_t)h * k_head_stride;
                     double dot = 0.0;
                     for (int e = 0; e < d; ++e) dot += bf16_value(q[e]) * bf16_value(k[e]);
-                    s[j] = c->sm_scale * dot;
+                    s[j] = (ORACLE_MUTANT == 1 ? 1.0 : c->sm_scale) * dot;
                     if (s[j] > mx) mx = s[j];
                 }
                 double l = 0.0;
@@ -113,7 +121,7 @@ int snap_oracle_window_scores(const snap_oracle_config* c, int64_t S,
 
 void snap_oracle_maxpool(const double* x, int64_t n, int P, double* y)
 {
-    const int64_t r = P / 2;
+    const int64_t r = P / 2 + (ORACLE_MUTANT == 4);
     for (int64_t j = 0; j < n; ++j) {
         int64_t a = j - r < 0 ? 0 : j - r;
         int64_t b = j + r > n - 1 ? n - 1 : j + r;
@@ -135,7 +143,8 @@ static int by_score_then_pos(const void* a, const void* b)
     const scored_pos* y = (const scored_pos*)b;
     if (x->score > y->score) return -1;
     if (x->score < y->score) return 1;
-    return (x->pos > y->pos) - (x->pos < y->pos);
+    return ORACLE_MUTANT == 5 ? (x->pos < y->pos) - (x->pos > y->pos)
+                              : (x->pos > y->pos) - (x->pos < y->pos);
 }
 
 static int ascending_i32(const void* a, const void* b)
@@ -167,7 +176,7 @@ int64_t snap_oracle_select(const double* score, int64_t lo, int64_t hi, int64_t 
 
 int64_t snap_oracle_ring_slot(const snap_oracle_config* c, int64_t p)
 {
-    return (int64_t)c->L_sink + c->K + (p % c->L_recent);
+    return (ORACLE_MUTANT == 6 ? 0 : (int64_t)c->L_sink + c->K) + (p % c->L_recent);
 }
 
 static void copy_row(uint16_t* dst, const uint16_t* src, int n)
@@ -251,7 +260,7 @@ int snap_oracle_slot_valid(const snap_oracle_config* c, const snap_oracle_meta* 
 {
     if (s < 0) return 0;
     if (s < c->L_sink) return s < m->n_sink;
-    if (s < (int64_t)c->L_sink + c->K) return s - c->L_sink < m->n_mid;
+    if (s < (int64_t)c->L_sink + c->K) return ORACLE_MUTANT == 7 ? 1 : s - c->L_sink < m->n_mid;
     int64_t r = s - c->L_sink - c->K;
     if (r >= c->L_recent) return 0;
     int64_t n_ring, lo;
@@ -320,7 +329,7 @@ int snap_oracle_decode_attn(const snap_oracle_config* c, const uint16_t* cache_k
             /* GQA reads the V cache; MLA's value is the first d_v columns of the key row */
             const uint16_t* v = c->layout == 0 ? cache_v + ((int64_t)h * C + t) * dv
                                                : kh + t * dk;
-            for (int e = 0; e < dv; ++e) o[e] += p * bf16_value(v[e]);
+            for (int e = 0; e < dv; ++e) o[e] += p * bf16_value(v[ORACLE_MUTANT == 8 ? dv - 1 - e : e]);
         }
         for (int e = 0; e < dv; ++e) o[e] /= l;
     }
