@@ -2,7 +2,7 @@
 
 One step = one pass of the whole path over one batch: snap_compress of every
 sequence's prompt (window scoring, pooling, top-K, cache build), then D decode
-steps of snap_decode_append + snap_decode_attn over the fixed-size cache.
+steps over the fixed-size cache (snap_decode_step: ring append + split-KV attention).
 Inputs are seeded synthetic tensors already resident in HBM (the prefill K/V/Q
 of the batch and every decode step's q/k/v); they exceed the 129 MB L2 many
 times over, so no L2 flush is needed between steps.
@@ -33,6 +33,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode tok/s + HBM GB/s (fixed cache vs full KV) at 128k ctx; compress ms"
+L2_BYTES = 129 << 20
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -46,6 +47,8 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
+    p.add_argument("--graph", action="store_true",
+                   help="replay the decode loop as one captured CUDA graph (small workloads)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-full-kv", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
@@ -198,10 +201,11 @@ def run_ours(args):
         if ev is not None:
             ev["c1"].record(stream)
         for t in range(D):
-            c.decode_append(slots, k_all[t], v_all[t] if v_all is not None else None, stream=stream)
+            # one decode step: append the new token, then attend (snap_decode_step)
             if ev is not None:
                 ev["a0"][t].record(stream)
-            c.decode_attn(slots, q_all[t], out=out[t], stream=stream)
+            c.decode_step(slots, q_all[t], k_all[t], v_all[t] if v_all is not None else None, out=out[t],
+                          stream=stream)
             if ev is not None:
                 ev["a1"][t].record(stream)
         if ev is not None:
@@ -215,6 +219,18 @@ def run_ours(args):
     for _ in range(args.warmup):
         one_step(cache, pre)
     barrier()
+    graph = None
+    if args.graph:
+        # the decode loop has static shapes and no host synchronisation: capture it once
+        graph = torch.cuda.CUDAGraph()
+        for b in range(B):
+            cache.compress(b, pre[b].K, pre[b].V, pre[b].Q, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for t in range(D):
+                cache.decode_step(slots, q_all[t], k_all[t], v_all[t] if v_all is not None else None,
+                                  out=out[t], stream=stream)
+        stream.synchronize()
     st = cache.check_device(stream)
     if st != snap.SNAP_OK:
         raise RuntimeError(f"device status after warm-up: {snap.status_string(st)}")
@@ -224,22 +240,45 @@ def run_ours(args):
                  [(m[0], m[1], m[2], m[3], m[4]) for m in metas]]
     attn_bytes = algorithmic_decode_bytes(wl, mid_metas)
 
+    # working set of one step: prompts, cache, decode inputs and outputs
+    work_bytes = sum(p.K.numel() * 2 + (p.V.numel() * 2 if p.V is not None else 0) for p in pre)
+    work_bytes += snap.cache_bytes(cfg, B) + q_all.numel() * 2 + k_all.numel() * 2 + out.numel() * 4
+    flush = None
+    if work_bytes < 4 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     clocks = ClockSampler(local)
     clocks.start()
     evs = [new_events() for _ in range(args.steps)]
     barrier()
     t_wall = time.perf_counter()
     for i in range(args.steps):
+        if flush is not None:  # evict the previous step's data from L2 (not timed)
+            with torch.cuda.stream(stream):
+                flush.fill_(i & 255)
         evs[i]["s0"].record(stream)
-        one_step(cache, pre, evs[i])
+        if graph is None:
+            one_step(cache, pre, evs[i])
+        else:
+            evs[i]["c0"].record(stream)
+            for b in range(B):
+                cache.compress(b, pre[b].K, pre[b].V, pre[b].Q, stream=stream)
+            evs[i]["c1"].record(stream)
+            with torch.cuda.stream(stream):  # replay on the stream the events are recorded on
+                graph.replay()
+            evs[i]["d1"].record(stream)
     barrier()
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
     step_ms = [evs[i]["s0"].elapsed_time(evs[i]["d1"]) for i in range(args.steps)]
     compress_ms = [evs[i]["c0"].elapsed_time(evs[i]["c1"]) for i in range(args.steps)]
     decode_ms = [evs[i]["c1"].elapsed_time(evs[i]["d1"]) for i in range(args.steps)]
-    attn_ms = [sum(evs[i]["a0"][t].elapsed_time(evs[i]["a1"][t]) for t in range(D)) / D
-               for i in range(args.steps)]
+    if graph is not None:
+        # per-launch attention time from one more pass of the same calls, launched one by one
+        ev = new_events()
+        one_step(cache, pre, ev)
+        stream.synchronize()
+        evs = [ev]
+    attn_ms = [sum(e["a0"][t].elapsed_time(e["a1"][t]) for t in range(D)) / D for e in evs]
     total_ms = sum(step_ms)
     st = cache.check_device(stream)
     if st != snap.SNAP_OK:
@@ -275,10 +314,10 @@ def run_ours(args):
             ea, eb = [], []
             e0.record(stream)
             for t in range(D):
-                fcache.decode_append(slots, k_all[t], v_all[t] if v_all is not None else None, stream=stream)
                 a, bb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                fcache.decode_attn(slots, q_all[t], out=out[t], stream=stream)
+                fcache.decode_step(slots, q_all[t], k_all[t], v_all[t] if v_all is not None else None,
+                                   out=out[t], stream=stream)
                 bb.record(stream)
                 ea.append(a)
                 eb.append(bb)
@@ -315,8 +354,8 @@ def run_ours(args):
     for S in lengths:
         M = (max(wl.L_sink, S - wl.L_recent) if S > wl.L_sink else S) - min(S, wl.L_sink)
         per_step_launches += n_seq_launch if (M > wl.K and wl.K > 0) else 1
-    splits_merge = 1  # decode merge kernel (split-KV) launches per decode step
-    per_step_launches += D * (2 + splits_merge)
+    # decode launches per step: append, attention, split merge
+    per_step_launches += D * 3
     traffic = traffic_record(wl.name)
     line = {
         "metric": METRIC,
@@ -334,7 +373,10 @@ def run_ours(args):
         "config": {"workload": wl.name, "batch": B, "prompt_len": max(lengths), "decode_steps": D,
                    "cache": f"{wl.L_sink}+{wl.K}+{wl.L_recent}={wl.C}", "W": wl.W, "P": wl.P,
                    "heads": f"{wl.n_q_heads}/{wl.n_kv_heads}x{wl.d_qk}",
-                   "parallelism": f"replicas x{world}", "l2": "inputs larger than L2 (no flush)"},
+                   "parallelism": f"replicas x{world}",
+                   "l2": ("inputs larger than L2 (no flush)" if flush is None
+                          else f"L2 flushed before each step ({2 * L2_BYTES >> 20} MiB write)"),
+                   "decode_launch": "cuda graph" if graph is not None else "eager"},
         "decode_tok_s": B * D * world / (dec_ms / 1e3),
         "decode_ms_per_token_step": dec_ms / D,
         "compress_ms_per_batch": cmp_ms,
@@ -343,7 +385,7 @@ def run_ours(args):
         "full_kv": full,
         "speedup_vs_full_kv": (B * D * world / (dec_ms / 1e3)) / full["decode_tok_s"] if full else None,
         "cache_bytes": snap.cache_bytes(cfg, B),
-        "roofline": {"bound": "hbm", "kernel": "snap_decode_attn (gqa decode + split merge)",
+        "roofline": {"bound": "hbm", "kernel": "snap_decode_step (append + split-KV attention + merge)",
                      "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": attn_gbs / hbm_peak, "peak_source": peak_kind,
                      "traffic": traffic},
@@ -413,8 +455,7 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
                 dk.copy_(hk[t], non_blocking=True)
                 if dv is not None:
                     dv.copy_(hv[t], non_blocking=True)
-                cache.decode_append(slots, dk, dv, stream=stream)
-                cache.decode_attn(slots, dq, out=dout, stream=stream)
+                cache.decode_step(slots, dq, dk, dv, out=dout, stream=stream)
                 hout[t].copy_(dout, non_blocking=True)
     steps = max(1, min(args.steps, 3))
     step()
@@ -587,8 +628,8 @@ def run_mixed(args):
             n = len(active)
             if n:
                 tk = toks[t % 64]
-                cache.decode_append(slots_t, tk.k[:n], tk.v[:n] if tk.v is not None else None, stream=sa)
-                cache.decode_attn(slots_t, tk.q[:n], out=out[:n], stream=sa)
+                cache.decode_step(slots_t, tk.q[:n], tk.k[:n], tk.v[:n] if tk.v is not None else None,
+                                  out=out[:n], stream=sa)
                 tokens += n
                 done = False
                 for s in active:

@@ -15,6 +15,8 @@
 // col(j) = sum_r 2^(s_rj - lse2(r)).  select (here) pools, finds the K-th largest
 // by radix descent and compacts the kept positions in order.  Scores s are in the
 // base-2 domain: s = sm_scale * log2(e) * q.k.
+#include <cooperative_groups.h>
+
 #include "kernels.cuh"
 
 namespace snap {
@@ -43,13 +45,18 @@ __global__ void lse_merge_kernel(CompressArgs a) {
 }
 
 // ------------------------------------------------------------------- select
-// One CTA of 1024 threads per KV head.  Pooled scores (non-negative floats,
-// compared as their IEEE bit patterns, which order them) of the middle
-// positions; the K-th largest found by a 4 x 8-bit radix descent; then an
-// ordered compaction keeps every score above it and the lowest-position ties.
+// One cluster of SEL_CLUSTER CTAs per KV head; CTA r owns a contiguous slice of
+// the middle positions.  Pooled scores (non-negative floats, compared as their
+// IEEE bit patterns, which order them) are written once; the K-th largest is
+// found by a 4 x 8-bit radix descent whose per-CTA histograms are summed through
+// distributed shared memory; an ordered compaction then keeps every score above
+// it and, among the scores equal to it, the lowest positions.
 constexpr int SEL_THREADS = 1024;
+constexpr int SEL_WARPS = SEL_THREADS / 32;
+constexpr int SEL_CLUSTER = 8;
 
-__device__ __forceinline__ int block_excl_scan(int x, int* warp_tot, int& total) {
+// Exclusive prefix sum over the block; *total receives the block sum.
+__device__ __forceinline__ int block_excl_scan(int x, int* warp_tot, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = x;
 #pragma unroll
@@ -60,67 +67,99 @@ __device__ __forceinline__ int block_excl_scan(int x, int* warp_tot, int& total)
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
     if (warp == 0) {
-        int v = lane < (SEL_THREADS / 32) ? warp_tot[lane] : 0;
+        const int v = warp_tot[lane];
         int vi = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, vi, o);
             if (lane >= o) vi += y;
         }
-        warp_tot[lane] = vi - v;        // exclusive prefix of warp totals
+        warp_tot[lane] = vi - v;
         if (lane == 31) warp_tot[32] = vi;
     }
     __syncthreads();
     const int r = warp_tot[warp] + incl - x;
-    total = warp_tot[32];
+    *total = warp_tot[32];
     __syncthreads();
     return r;
 }
 
-__global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a) {
-    __shared__ int hist[256];
+__global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 1)
+    select_kernel(CompressArgs a) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ int hist_w[SEL_WARPS][256];       // per-warp private histograms
+    __shared__ int hist_cta[2][256];             // this CTA's histogram, double-buffered by pass
     __shared__ int warp_tot[33];
+    __shared__ int counts[2];                    // this CTA's (greater, equal) counts
     __shared__ uint32_t sh_prefix;
     __shared__ int sh_kk;
     const DevConfig& c = a.cfg;
-    const int h = blockIdx.x;
+    const int h = blockIdx.y;
+    const int rank = (int)cluster.block_rank();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_sc = a.S - c.W;
-    const int M = a.R0 - c.L_sink;        // middle candidates [L_sink, R0)
-    const int r = c.P / 2;
-    // the score GEMM leaves each column sum as two halves (two groups of rows)
+    const int M = a.R0 - c.L_sink;               // middle candidates [L_sink, R0)
+    const int rad = c.P / 2;
+    const int per = (M + SEL_CLUSTER - 1) / SEL_CLUSTER;
+    const int i0 = min(M, rank * per), i1 = min(M, i0 + per);
     const float* c0 = a.col + (size_t)h * a.S_pad;
     const float* c1 = a.col + ((size_t)c.Hkv + h) * a.S_pad;
     uint32_t* pool = a.pool + (size_t)h * a.S_pad;
 
-    for (int i = threadIdx.x; i < M; i += SEL_THREADS) {
+    // 0. pooled scores of this slice (the score GEMM leaves each column sum in two halves)
+    for (int i = i0 + tid; i < i1; i += SEL_THREADS) {
         const int j = c.L_sink + i;
-        const int lo = max(0, j - r), hi = min(n_sc - 1, j + r);
+        const int lo = max(0, j - rad), hi = min(n_sc - 1, j + rad);
         float mx = c0[lo] + c1[lo];
         for (int k = lo + 1; k <= hi; ++k) mx = fmaxf(mx, c0[k] + c1[k]);
         pool[i] = __float_as_uint(mx);
     }
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         sh_prefix = 0u;
         sh_kk = c.K;
     }
     __syncthreads();
 
+    // 1-4. radix descent over the whole middle, 8 bits at a time
     uint32_t mask = 0u;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        for (int i = threadIdx.x; i < 256; i += SEL_THREADS) hist[i] = 0;
-        __syncthreads();
         const uint32_t prefix = sh_prefix;
-        for (int i = threadIdx.x; i < M; i += SEL_THREADS) {
-            const uint32_t v = pool[i];
-            if ((v & mask) == prefix) atomicAdd(&hist[(v >> shift) & 255u], 1);
+        for (int i = lane; i < 256; i += 32) hist_w[warp][i] = 0;
+        __syncwarp();
+        for (int base = i0; base < i1; base += SEL_THREADS) {
+            const int i = base + tid;
+            const bool in = i < i1;
+            const uint32_t v = in ? pool[i] : 0u;
+            const bool match = in && (v & mask) == prefix;
+            const unsigned active = __ballot_sync(0xffffffffu, match);
+            if (match) {
+                const int d = (int)((v >> shift) & 255u);
+                const unsigned same = __match_any_sync(active, d);
+                if ((int)(__ffs(same) - 1) == lane) atomicAdd(&hist_w[warp][d], __popc(same));
+            }
         }
         __syncthreads();
-        if (threadIdx.x == 0) {
+        int* hc = hist_cta[pass & 1];
+        for (int d = tid; d < 256; d += SEL_THREADS) {
+            int t = 0;
+            for (int w = 0; w < SEL_WARPS; ++w) t += hist_w[w][d];
+            hc[d] = t;
+        }
+        cluster.sync();                          // every CTA's histogram of this pass is ready
+        __shared__ int hist_all[256];
+        for (int d = tid; d < 256; d += SEL_THREADS) {
+            int t = 0;
+            for (int r = 0; r < SEL_CLUSTER; ++r) t += cluster.map_shared_rank(hc, r)[d];
+            hist_all[d] = t;
+        }
+        __syncthreads();
+        if (tid == 0) {
             int kk = sh_kk, cum = 0, d = 255;
             for (; d > 0; --d) {
-                if (cum + hist[d] >= kk) break;
-                cum += hist[d];
+                if (cum + hist_all[d] >= kk) break;
+                cum += hist_all[d];
             }
             sh_kk = kk - cum;
             sh_prefix = prefix | ((uint32_t)d << shift);
@@ -129,27 +168,74 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a) 
         __syncthreads();
     }
     const uint32_t tau = sh_prefix;
-    const int kk = sh_kk;                 // how many scores equal to tau are kept
+    const int kk = sh_kk;                        // how many scores equal to tau are kept
 
-    int32_t* out = a.sel + ((size_t)a.slot * c.Hkv + h) * c.K;
-    int eq_before = 0, taken_before = 0;
-    for (int base = 0; base < M; base += SEL_THREADS) {
-        const int i = base + threadIdx.x;
-        const uint32_t v = i < M ? pool[i] : 0u;
-        const int gt = (i < M && v > tau) ? 1 : 0;
-        const int eq = (i < M && v == tau) ? 1 : 0;
-        int eq_tot;
-        const int eq_rank = block_excl_scan(eq, warp_tot, eq_tot);
-        const int take = gt | (eq && (eq_before + eq_rank) < kk);
-        int take_tot;
-        const int pos = block_excl_scan(take, warp_tot, take_tot);
-        if (take) out[taken_before + pos] = c.L_sink + i;
-        eq_before += eq_tot;
-        taken_before += take_tot;
+    // 5. ordered compaction: thread t scans a contiguous run of this slice
+    const int run = (i1 - i0 + SEL_THREADS - 1) / SEL_THREADS;
+    const int r0 = min(i1, i0 + tid * run), r1 = min(i1, r0 + run);
+    int gt = 0, eq = 0;
+    for (int i = r0; i < r1; ++i) {
+        const uint32_t v = pool[i];
+        gt += v > tau;
+        eq += v == tau;
     }
+    int gt_cta, eq_cta;
+    const int gt_before = block_excl_scan(gt, warp_tot, &gt_cta);
+    const int eq_before = block_excl_scan(eq, warp_tot, &eq_cta);
+    if (tid == 0) {
+        counts[0] = gt_cta;
+        counts[1] = eq_cta;
+    }
+    cluster.sync();
+    // positions kept by lower-ranked CTAs, and equal scores met before this slice
+    int taken_prev = 0, eq_prev = 0;
+    for (int r = 0; r < rank; ++r) {
+        const int* cr = cluster.map_shared_rank(counts, r);
+        const int g = cr[0], e = cr[1];
+        taken_prev += g + min(max(kk - eq_prev, 0), e);
+        eq_prev += e;
+    }
+    int32_t* out = a.sel + ((size_t)a.slot * c.Hkv + h) * c.K;
+    // this thread's first output index: greater ones before it in the slice, plus the
+    // equal ones before it that are kept
+    const int eq_g = eq_prev + eq_before;       // equal scores before this thread's run
+    int pos = taken_prev + gt_before + min(max(kk - eq_prev, 0), eq_before);
+    int e_seen = eq_g;
+    for (int i = r0; i < r1; ++i) {
+        const uint32_t v = pool[i];
+        bool take = v > tau;
+        if (v == tau) {
+            take = e_seen < kk;
+            ++e_seen;
+        }
+        if (take) out[pos++] = c.L_sink + i;
+    }
+    cluster.sync();                              // peers may still read this CTA's counters
 }
 
 }  // namespace
+
+namespace {
+// Row r = w*G + g of KV head h is query head h*G + g at window position w; the
+// caller's LSE is natural-log: -lse2 = -lse * log2(e).
+__global__ void lse_import_kernel(CompressArgs a, const float* lse_obs) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;   // over Hkv * R_pad
+    if (i >= a.cfg.Hkv * a.R_pad) return;
+    const int h = i / a.R_pad, r = i % a.R_pad;
+    if (r >= a.R) {
+        a.nlse2[i] = NEG_INF;
+        return;
+    }
+    const int w = r / a.cfg.G, g = r % a.cfg.G;
+    a.nlse2[i] = -lse_obs[(size_t)w * a.cfg.Hq + (size_t)h * a.cfg.G + g] * 1.4426950408889634f;
+}
+}  // namespace
+
+cudaError_t launch_lse_import(const CompressArgs& a, const float* lse_obs, cudaStream_t st) {
+    const int total = a.cfg.Hkv * a.R_pad;
+    lse_import_kernel<<<(total + 255) / 256, 256, 0, st>>>(a, lse_obs);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_lse_merge(const CompressArgs& a, cudaStream_t st) {
     const int total = a.cfg.Hkv * a.R_pad;
@@ -158,7 +244,8 @@ cudaError_t launch_lse_merge(const CompressArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_select(const CompressArgs& a, cudaStream_t st) {
-    select_kernel<<<a.cfg.Hkv, SEL_THREADS, 0, st>>>(a);
+    dim3 grid(SEL_CLUSTER, a.cfg.Hkv);
+    select_kernel<<<grid, SEL_THREADS, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -2,7 +2,7 @@
 //
 // SnapStream episode companion page, "Prefill / Decode Pipeline": decode is
 // memory-bound, so the cache bytes streamed per step set the time per token.
-// Each CTA streams one contiguous range of cache slots of one (sequence, KV head)
+// GQA: each CTA streams one contiguous range of cache slots of one (sequence, KV head)
 // once from HBM and produces an un-normalised partial (max, sum, O) per query
 // head; a merge kernel combines the splits (flash-decoding's log-sum-exp merge).
 // Invalid slots (unused middle slots, ring slots not holding a live position)
@@ -251,221 +251,6 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
     }
 }
 
-// ===================================================================== MLA
-// Key row = [latent 512 | rope 64]; value = latent.  One CTA: 16 query heads of
-// one sequence over a range of 64-key tiles.  Warp w computes the scores of keys
-// 16w..16w+15 (all 576 columns); the softmax runs on shared memory; warp w then
-// accumulates O[:, 128w : 128w+128] = P V.
-constexpr int MK = 576, MV = 512;
-constexpr int M_ROWB = MK * 2;                        // 1152 bytes
-constexpr int M_STAGES = 2;
-constexpr int M_TILE_BYTES = MLA_KEYS * M_ROWB;       // 72 KB
-constexpr int M_Q_BYTES = MLA_HB * M_ROWB;            // 18 KB
-constexpr int M_S_BYTES = MLA_HB * MLA_KEYS * 4;      // 4 KB scores
-constexpr int M_P_BYTES = MLA_HB * MLA_KEYS * 2;      // 2 KB probabilities (bf16)
-constexpr int M_SMEM = M_STAGES * M_TILE_BYTES + M_Q_BYTES + M_S_BYTES + M_P_BYTES + 3 * MLA_HB * 4;
-
-__global__ void __launch_bounds__(128, 1) mla_decode_kernel(DecodeArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const DevConfig& c = a.cfg;
-    const int hb = blockIdx.x, split = blockIdx.y, b = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slot = a.slots[b];
-    if (slot < 0 || slot >= c.max_batch) {
-        if (tid == 0 && split == 0 && hb == 0) report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
-        if (a.splits == 1)
-            for (int i = tid; i < MLA_HB * MV; i += blockDim.x)
-                a.out[((size_t)b * c.Hq + (size_t)hb * MLA_HB) * MV + i] = 0.f;
-        return;
-    }
-    const snap_seq_meta m = a.meta[slot];
-    SlotValidity sv;
-    sv.init(m, c);
-    const bf16* kvbase = a.kc + (size_t)slot * c.C * MK;
-
-    const uint32_t s_kv = smem_u32(smem);
-    const uint32_t s_q = s_kv + M_STAGES * M_TILE_BYTES;
-    float* S = reinterpret_cast<float*>(smem + M_STAGES * M_TILE_BYTES + M_Q_BYTES);
-    const uint32_t s_p = s_q + M_Q_BYTES + M_S_BYTES;
-    float* m_s = reinterpret_cast<float*>(smem + M_STAGES * M_TILE_BYTES + M_Q_BYTES + M_S_BYTES + M_P_BYTES);
-    float* l_s = m_s + MLA_HB;
-    float* al_s = l_s + MLA_HB;
-
-    // Q block -> shared (swizzled rows of 72 chunks)
-    {
-        const bf16* qp = a.q + ((size_t)b * c.Hq + (size_t)hb * MLA_HB) * MK;
-        for (int i = tid; i < MLA_HB * 72; i += 128) {
-            const int r = i / 72, ch = i % 72;
-            cp_async16(s_q + swz(r, ch, M_ROWB), qp + (size_t)r * MK + ch * 8);
-        }
-        cp_async_commit();
-    }
-    if (tid < MLA_HB) {
-        m_s[tid] = NEG_INF;
-        l_s[tid] = 0.f;
-    }
-
-    const int ntiles = (c.C + MLA_KEYS - 1) / MLA_KEYS;
-    const int t_begin = split * a.tiles_per_split;
-    const int t_end = min(ntiles, t_begin + a.tiles_per_split);
-    auto next_tile = [&](int t) {
-        while (t < t_end && !sv.any_valid(t * MLA_KEYS, min(c.C, (t + 1) * MLA_KEYS))) ++t;
-        return t;
-    };
-    auto load_tile = [&](int t, int st) {
-        const uint32_t dst = s_kv + st * M_TILE_BYTES;
-        for (int i = tid; i < MLA_KEYS * 72; i += 128) {
-            const int r = i / 72, ch = i % 72;
-            const int key = t * MLA_KEYS + r;
-            const bool ok = key < c.C;
-            cp_async16(dst + swz(r, ch, M_ROWB), kvbase + (size_t)(ok ? key : 0) * MK + ch * 8,
-                       ok ? 16 : 0);
-        }
-    };
-
-    float o[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
-    int t_load = next_tile(t_begin), t_comp = t_load;
-    if (t_load < t_end) {
-        load_tile(t_load, 0);
-        t_load = next_tile(t_load + 1);
-    }
-    cp_async_commit();
-    int st = 0;
-    const float sl2 = c.scale_log2;
-    while (t_comp < t_end) {
-        if (t_load < t_end) {
-            load_tile(t_load, st ^ 1);
-            t_load = next_tile(t_load + 1);
-        }
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        const uint32_t kv = s_kv + st * M_TILE_BYTES;
-        // ---- scores S[16 heads][keys 16w .. 16w+15]
-        {
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 4
-            for (int ks = 0; ks < MK / 16; ++ks) {
-                uint32_t af[4], bfr[4];
-                const int ar = (lane & 7) + (((lane >> 3) & 1) << 3);
-                ldsm_x4(s_q + swz(ar, ks * 2 + (lane >> 4), M_ROWB), af[0], af[1], af[2], af[3]);
-                const int br = warp * 16 + (lane & 7) + ((lane >> 4) << 3);
-                ldsm_x4(kv + swz(br, ks * 2 + ((lane >> 3) & 1), M_ROWB), bfr[0], bfr[1], bfr[2], bfr[3]);
-                mma_bf16(acc[0], af, bfr[0], bfr[1]);
-                mma_bf16(acc[1], af, bfr[2], bfr[3]);
-            }
-            const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int kl = warp * 16 + nt * 8 + 2 * t + (i & 1);
-                    const int row = g + 8 * (i >> 1);
-                    const int key = t_comp * MLA_KEYS + kl;
-                    const bool ok = key < c.C && sv.valid(key);
-                    S[row * MLA_KEYS + kl] = ok ? acc[nt][i] * sl2 : NEG_INF;
-                }
-        }
-        __syncthreads();
-        // ---- online softmax: thread = (row tid/8, 8 keys)
-        {
-            const int row = tid >> 3, seg = tid & 7;
-            float v[8];
-            float mx = NEG_INF;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                v[i] = S[row * MLA_KEYS + seg * 8 + i];
-                mx = fmaxf(mx, v[i]);
-            }
-#pragma unroll
-            for (int x = 1; x < 8; x <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
-            const float mo = m_s[row];
-            const float mn = fmaxf(mo, mx);
-            const float al = mn == NEG_INF ? 1.f : ex2(mo - mn);
-            float sum = 0.f;
-            uint32_t pk[4];
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                const float p0 = mn == NEG_INF ? 0.f : bf16_round(ex2(v[i] - mn));
-                const float p1 = mn == NEG_INF ? 0.f : bf16_round(ex2(v[i + 1] - mn));
-                sum += p0 + p1;
-                pk[i / 2] = pack_bf16(p0, p1);
-            }
-#pragma unroll
-            for (int x = 1; x < 8; x <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, x);
-            const uint32_t dst = s_p + swz(row, seg, MLA_KEYS * 2);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst), "r"(pk[0]), "r"(pk[1]),
-                         "r"(pk[2]), "r"(pk[3]));
-            __syncwarp();
-            if (seg == 0) {
-                m_s[row] = mn;
-                l_s[row] = l_s[row] * al + sum;
-                al_s[row] = al;
-            }
-        }
-        __syncthreads();
-        // ---- O[:, 128w : 128w+128] = O * alpha + P V
-        {
-            const int g = lane >> 2;
-            const float a0 = al_s[g], a1 = al_s[g + 8];
-#pragma unroll
-            for (int nt = 0; nt < 16; ++nt) {
-                o[nt][0] *= a0;
-                o[nt][1] *= a0;
-                o[nt][2] *= a1;
-                o[nt][3] *= a1;
-            }
-#pragma unroll
-            for (int ks = 0; ks < MLA_KEYS / 16; ++ks) {
-                uint32_t af[4];
-                const int ar = (lane & 7) + (((lane >> 3) & 1) << 3);
-                ldsm_x4(s_p + swz(ar, ks * 2 + (lane >> 4), MLA_KEYS * 2), af[0], af[1], af[2], af[3]);
-#pragma unroll
-                for (int nt = 0; nt < 16; nt += 2) {
-                    uint32_t bfr[4];
-                    const int key = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-                    const int ch = warp * 16 + nt + (lane >> 4);
-                    ldsm_x4_t(kv + swz(key, ch, M_ROWB), bfr[0], bfr[1], bfr[2], bfr[3]);
-                    mma_bf16(o[nt], af, bfr[0], bfr[1]);
-                    mma_bf16(o[nt + 1], af, bfr[2], bfr[3]);
-                }
-            }
-        }
-        __syncthreads();  // stage and S/P buffers are reused next iteration
-        t_comp = next_tile(t_comp + 1);
-        st ^= 1;
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-
-    // write this split's result
-    const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int row = g + 8 * (i >> 1);
-            const int d = warp * 128 + nt * 8 + 2 * t + (i & 1);
-            const int head = hb * MLA_HB + row;
-            if (a.splits == 1) {
-                const float L = l_s[row];
-                const float r = L > 0.f ? o[nt][i] / L : 0.f;
-                a.out[((size_t)b * c.Hq + head) * MV + d] = r;
-            } else {
-                const size_t pi = ((size_t)b * a.splits + split) * c.Hq + head;
-                a.part_o[pi * MV + d] = o[nt][i];
-            }
-        }
-    if (a.splits > 1 && tid < MLA_HB) {
-        const size_t pi = ((size_t)b * a.splits + split) * c.Hq + hb * MLA_HB + tid;
-        a.part_ml[pi * 2 + 0] = m_s[tid];
-        a.part_ml[pi * 2 + 1] = l_s[tid];
-    }
-}
-
 // =================================================================== merge
 // out[b][i][:] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s  (zero if empty).
 // Partial index: ((b * Hkv + h) * splits + s) * G + hh  for query head i = h*G + hh.
@@ -510,19 +295,6 @@ cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st) {
     }
     dim3 grid(a.splits, a.cfg.Hkv, a.n);
     gqa_decode_kernel<<<grid, G_WARPS * 32, G_SMEM, st>>>(a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_decode_mla(const DecodeArgs& a, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, M_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    dim3 grid(a.cfg.Hq / MLA_HB, a.splits, a.n);
-    mla_decode_kernel<<<grid, 128, M_SMEM, st>>>(a);
     return cudaGetLastError();
 }
 

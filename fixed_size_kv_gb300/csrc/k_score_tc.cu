@@ -53,11 +53,28 @@ struct Layout {
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && *abort_flag) return false;
-    }
-    return false;
+    return mbar_wait_bounded(bar, parity, abort_flag, false);
+}
+
+// sum_i 2^(v_i * a + b) over 32 values, with independent partial sums
+__device__ __forceinline__ float sum32_ex2(const float (&v)[32], float a, float b) {
+    float t[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = ex2(fmaf(v[k], a, b));
+#pragma unroll
+    for (int i = 8; i < 32; i += 8)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) t[k] += ex2(fmaf(v[i + k], a, b));
+    return ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+}
+
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+    float t[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = fmaxf(v[k], v[k + 8]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = fmaxf(t[k], fmaxf(v[k + 16], v[k + 24]));
+    return fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
 }
 
 struct Unit {
@@ -266,7 +283,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int s = 0; s < U.nsteps; ++s, ++acc_it) {
                 const int buf = acc_it & 1;
                 const uint32_t na = acc_it >> 1;
-                if (!wait_or_abort(bar(B_ACC_FULL + buf), na & 1, abort_flag)) { fail(2, u); goto epi_done; }
+                // warp-uniform exit: the TMEM loads below are warp-collective
+                if (!__all_sync(0xffffffffu, wait_or_abort(bar(B_ACC_FULL + buf), na & 1, abort_flag))) {
+                    fail(2, u);
+                    goto epi_done;
+                }
                 tc_fence_after();
                 const int y0 = (XRES ? (U.yt0 + s) : U.yt0) * Ny;   // first column's key / row index
                 // -lse2 of the observation rows on this tile's columns (same for every lane)
@@ -283,29 +304,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int i = 0; i < 32; ++i)
                                 if (key0 + i > pos) v[i] = NEG_INF;
                         }
-                        float mx = v[0];
-#pragma unroll
-                        for (int i = 1; i < 32; ++i) mx = fmaxf(mx, v[i]);
-                        const float mn = fmaxf(m, mx * sl2);
-                        if (mn != NEG_INF) {
-                            float sum = 0.f;
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) sum += ex2(fmaf(v[i], sl2, -mn));
-                            l = l * ex2(m - mn) + sum;
-                            m = mn;
+                        // The reference m is kept lazily: it is set from a chunk's true
+                        // maximum only when it is still -inf or when the chunk's sum against
+                        // it leaves [0, 2^32] (a logit more than ~27 above m, or overflow).
+                        // l * 2^m is exact either way.
+                        float sum = 0.f;
+                        bool redo = (m == NEG_INF);
+                        if (!redo) {
+                            sum = sum32_ex2(v, sl2, -m);
+                            redo = !(sum <= 4294967296.f);
                         }
+                        if (redo) {
+                            float mx = max32(v) * sl2;
+                            const float mn = fmaxf(m, mx);
+                            if (mn != NEG_INF) {
+                                sum = sum32_ex2(v, sl2, -mn);
+                                l = l * ex2(m - mn);
+                                m = mn;
+                            } else {
+                                sum = 0.f;
+                            }
+                        }
+                        l += sum;
                     } else if (MODE == COLSUM) {
                         const float4* nl4 = reinterpret_cast<const float4*>(nl + col0);
-                        float sum = 0.f;
+                        float s4[4] = {0.f, 0.f, 0.f, 0.f};   // independent accumulators
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float4 b = __ldg(nl4 + i);
-                            sum += ex2(fmaf(v[4 * i + 0], sl2, b.x));
-                            sum += ex2(fmaf(v[4 * i + 1], sl2, b.y));
-                            sum += ex2(fmaf(v[4 * i + 2], sl2, b.z));
-                            sum += ex2(fmaf(v[4 * i + 3], sl2, b.w));
+                            s4[0] += ex2(fmaf(v[4 * i + 0], sl2, b.x));
+                            s4[1] += ex2(fmaf(v[4 * i + 1], sl2, b.y));
+                            s4[2] += ex2(fmaf(v[4 * i + 2], sl2, b.z));
+                            s4[3] += ex2(fmaf(v[4 * i + 3], sl2, b.w));
                         }
-                        acc += sum;
+                        acc += (s4[0] + s4[1]) + (s4[2] + s4[3]);
                     } else {  // LOGITS
                         if (r < p.R) {
                             float* o = p.logits + ((size_t)U.h * p.R + r) * p.S;

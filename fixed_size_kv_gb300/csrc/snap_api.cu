@@ -203,6 +203,13 @@ cudaError_t run_rowstat(int mode, const snap_config& c, ScoreParams sp, const vo
     return launch_score_tc(mode, tx, ty, sp, c.d_qk, true, true, num_sms(), st);
 }
 
+// MLA decode tensor maps: queries [n][128][576] (box 64 x 128) and the cache rows
+// [max_batch][C][576] (box 64 x 64).
+bool mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int n, const snap_cache* cache);
+
+// Split count and launches of one decode-attention call (shared by the entry points).
+cudaError_t run_decode(snap_cache* cache, DecodeArgs& a, cudaStream_t st);
+
 size_t decode_ws_bytes(const snap_config& c, int max_n) {
     const size_t parts = (size_t)max_n * c.n_q_heads * MAX_DECODE_SPLITS;
     return align_up(parts * sizeof(float) * c.d_v, 256) + align_up(parts * sizeof(float) * 2, 256);
@@ -220,7 +227,7 @@ snap_status check_config(const snap_config* c) {
     if ((int64_t)c->L_sink + c->K + c->L_recent > (1ll << 30)) return SNAP_ERR_SHAPE;
     if (c->layout == SNAP_LAYOUT_MLA) {
         if (c->n_kv_heads != 1 || c->d_v > c->d_qk) return SNAP_ERR_SHAPE;
-        if (c->d_qk != 576 || c->d_v != 512 || c->n_q_heads % MLA_HB) return SNAP_ERR_UNSUPPORTED;
+        if (c->d_qk != 576 || c->d_v != 512 || c->n_q_heads != MLA_HEADS) return SNAP_ERR_UNSUPPORTED;
     } else {
         if (c->d_qk != 128 || c->d_v != 128) return SNAP_ERR_UNSUPPORTED;
         if (c->n_q_heads / c->n_kv_heads > 8) return SNAP_ERR_UNSUPPORTED;
@@ -255,6 +262,48 @@ int decode_splits(int base, int tiles, int ctas_per_sm) {
         }
     }
     return best;
+}
+
+// Splits of one decode-attention call: enough CTAs for whole waves (GQA: 4 warps walk
+// a split, one 32-key tile each per step; MLA: two CTAs per split, 64-key tiles).
+int decode_split_count(const snap_cache* cache, int n) {
+    const snap_config& c = cache->cfg;
+    if (c.layout == SNAP_LAYOUT_GQA) {
+        const int tiles = (int)((cache->C + GQA_KEYS - 1) / GQA_KEYS);
+        return decode_splits(n * c.n_kv_heads, tiles / 4, 1);
+    }
+    const int tiles = (int)((cache->C + MLA_KEYS - 1) / MLA_KEYS);
+    return decode_splits(2 * n, tiles, 1);
+}
+
+int decode_tiles_per_split(const snap_cache* cache, int splits) {
+    const int key_tile = cache->cfg.layout == SNAP_LAYOUT_GQA ? GQA_KEYS : MLA_KEYS;
+    const int tiles = (int)((cache->C + key_tile - 1) / key_tile);
+    return (tiles + splits - 1) / splits;
+}
+
+bool mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int n, const snap_cache* cache) {
+    const snap_config& c = cache->cfg;
+    const cuuint64_t qd[3] = {(cuuint64_t)c.d_qk, (cuuint64_t)c.n_q_heads, (cuuint64_t)n};
+    const cuuint64_t qs[2] = {(cuuint64_t)c.d_qk * 2, (cuuint64_t)c.n_q_heads * c.d_qk * 2};
+    const cuuint32_t qb[3] = {64, (cuuint32_t)MLA_HEADS, 1};
+    const cuuint64_t kd[3] = {(cuuint64_t)c.d_qk, (cuuint64_t)cache->C, (cuuint64_t)cache->max_batch};
+    const cuuint64_t ks[2] = {(cuuint64_t)c.d_qk * 2, (cuuint64_t)cache->C * c.d_qk * 2};
+    const cuuint32_t kb[3] = {64, (cuuint32_t)MLA_KEYS, 1};
+    return encode(tq, q, 3, qd, qs, qb) && encode(tkv, cache->k, 3, kd, ks, kb);
+}
+
+cudaError_t run_decode(snap_cache* cache, DecodeArgs& a, cudaStream_t st) {
+    cudaError_t e;
+    if (cache->cfg.layout == SNAP_LAYOUT_GQA) {
+        e = launch_decode_gqa(a, st);
+    } else {
+        CUtensorMap tq, tkv;
+        if (!mla_maps(&tq, &tkv, a.q, a.n, cache)) return cudaErrorInvalidValue;
+        e = launch_decode_mla_tc(a, tq, tkv, st);
+    }
+    if (e == cudaSuccess && a.splits > 1) e = launch_decode_merge(a, st);
+    return e;
 }
 
 }  // namespace
@@ -338,9 +387,14 @@ snap_status snap_compress_ws_bytes(const snap_config* cfg, int64_t S_max, size_t
     return SNAP_OK;
 }
 
-snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
-                          int64_t tok_stride, int64_t head_stride, const void* Q_obs, void* ws,
-                          size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Compression of one sequence; lse_obs (nullable) replaces the row pass.
+snap_status compress_impl(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
+                          int64_t tok_stride, int64_t head_stride, const void* Q_obs, const float* lse_obs,
+                          void* ws, size_t ws_bytes, void* stream) {
     if (!cache || !K || !Q_obs) return SNAP_ERR_INVALID_ARG;
     const snap_config& c = cache->cfg;
     if (slot < 0 || slot >= cache->max_batch) return SNAP_ERR_INVALID_ARG;
@@ -393,12 +447,18 @@ snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void
         a.S_pad = w.S_pad;
         a.R_pad = w.R_pad;
         ScoreParams sp = score_params(c, S, w, wb, cache->status);
-        // 1. row pass: partial log-sum-exp of every observation row
-        cudaError_t e = run_rowstat(SCORE_ROWSTAT, c, sp, K, S, tok_stride, head_stride, Q_obs, st);
-        // 2. merge into -lse2 per row
-        if (e == cudaSuccess) {
-            a.row_splits = 2 * row_key_splits(c, w.R, S);
-            e = launch_lse_merge(a, st);
+        cudaError_t e;
+        if (lse_obs) {
+            // 1-2. the caller's row log-sum-exp, in the base-2 domain the GEMM uses
+            e = launch_lse_import(a, lse_obs, st);
+        } else {
+            // 1. row pass: partial log-sum-exp of every observation row
+            e = run_rowstat(SCORE_ROWSTAT, c, sp, K, S, tok_stride, head_stride, Q_obs, st);
+            // 2. merge into -lse2 per row
+            if (e == cudaSuccess) {
+                a.row_splits = 2 * row_key_splits(c, w.R, S);
+                e = launch_lse_merge(a, st);
+            }
         }
         // 3. column pass: X = 128-key tiles, Y = observation rows
         if (e == cudaSuccess) {
@@ -426,6 +486,23 @@ snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void
         if (e != cudaSuccess) return cuda_status(e);
     }
     return cuda_status(launch_cache_write(a, num_sms(), st));
+}
+
+}  // namespace
+
+extern "C" {
+
+snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
+                          int64_t tok_stride, int64_t head_stride, const void* Q_obs, void* ws,
+                          size_t ws_bytes, void* stream) {
+    return compress_impl(cache, slot, K, V, S, tok_stride, head_stride, Q_obs, nullptr, ws, ws_bytes, stream);
+}
+
+snap_status snap_compress_lse(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
+                              int64_t tok_stride, int64_t head_stride, const void* Q_obs, const float* lse_obs,
+                              void* ws, size_t ws_bytes, void* stream) {
+    if (!lse_obs || (reinterpret_cast<uintptr_t>(lse_obs) & 3u)) return SNAP_ERR_INVALID_ARG;
+    return compress_impl(cache, slot, K, V, S, tok_stride, head_stride, Q_obs, lse_obs, ws, ws_bytes, stream);
 }
 
 snap_status snap_window_logits(snap_cache* cache, const void* K, int64_t S, int64_t tok_stride,
@@ -492,13 +569,9 @@ snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, con
     a.out = static_cast<float*>(out);
     a.status = cache->status;
     a.cfg = dev_config(c, cache->max_batch);
-    const int key_tile = c.layout == SNAP_LAYOUT_GQA ? GQA_KEYS : MLA_KEYS;
-    const int tiles = (int)((cache->C + key_tile - 1) / key_tile);
-    const int base = c.layout == SNAP_LAYOUT_GQA ? n * c.n_kv_heads : n * (c.n_q_heads / MLA_HB);
-    // GQA: each split is walked by 4 warps, one 32-key tile each per step
-    int splits = decode_splits(base, c.layout == SNAP_LAYOUT_GQA ? tiles / 4 : tiles, 1);
+    const int splits = decode_split_count(cache, n);
     a.splits = splits;
-    a.tiles_per_split = (tiles + splits - 1) / splits;
+    a.tiles_per_split = decode_tiles_per_split(cache, splits);
     if (splits > 1) {
         const size_t need = decode_ws_bytes(c, n);
         if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SNAP_ERR_INVALID_ARG;
@@ -506,10 +579,13 @@ snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, con
         a.part_o = static_cast<float*>(ws);
         a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align_up(parts * sizeof(float) * c.d_v, 256));
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = c.layout == SNAP_LAYOUT_GQA ? launch_decode_gqa(a, st) : launch_decode_mla(a, st);
-    if (e == cudaSuccess && splits > 1) e = launch_decode_merge(a, st);
-    return cuda_status(e);
+    return cuda_status(run_decode(cache, a, static_cast<cudaStream_t>(stream)));
+}
+
+snap_status snap_decode_step(snap_cache* cache, const int32_t* slots, int n, const void* q, const void* k_new,
+                             const void* v_new, void* out, void* ws, size_t ws_bytes, void* stream) {
+    snap_status s = snap_decode_append(cache, slots, n, k_new, v_new, stream);
+    return s != SNAP_OK ? s : snap_decode_attn(cache, slots, n, q, out, ws, ws_bytes, stream);
 }
 
 snap_status snap_check_device(snap_cache* cache, void* stream) {
@@ -585,12 +661,9 @@ extern "C" snap_status snap_decode_attn_noalloc(snap_cache* cache, const int32_t
     a.out = static_cast<float*>(out);
     a.status = cache->status;
     a.cfg = dev_config(c, cache->max_batch);
-    const int key_tile = c.layout == SNAP_LAYOUT_GQA ? GQA_KEYS : MLA_KEYS;
-    const int tiles = (int)((cache->C + key_tile - 1) / key_tile);
-    const int base = c.layout == SNAP_LAYOUT_GQA ? n * c.n_kv_heads : n * (c.n_q_heads / MLA_HB);
-    const int splits = decode_splits(base, c.layout == SNAP_LAYOUT_GQA ? tiles / 4 : tiles, 1);
+    const int splits = decode_split_count(cache, n);
     a.splits = splits;
-    a.tiles_per_split = (tiles + splits - 1) / splits;
+    a.tiles_per_split = decode_tiles_per_split(cache, splits);
     if (splits > 1) {
         // compact partial layout for this call: O then (max, sum)
         const size_t parts = (size_t)n * c.n_q_heads * splits;
@@ -609,8 +682,5 @@ extern "C" snap_status snap_decode_attn_noalloc(snap_cache* cache, const int32_t
         a.part_o = static_cast<float*>(scratch);
         a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + o_bytes);
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = c.layout == SNAP_LAYOUT_GQA ? launch_decode_gqa(a, st) : launch_decode_mla(a, st);
-    if (e == cudaSuccess && splits > 1) e = launch_decode_merge(a, st);
-    return cuda_status(e);
+    return cuda_status(run_decode(cache, a, static_cast<cudaStream_t>(stream)));
 }

@@ -58,10 +58,12 @@ SIGNATURES = {
     "snap_cache_view_get": (_I, [_VP, _P(snap_cache_view)]),
     "snap_compress_ws_bytes": (_I, [_P(snap_config), _I64, _P(_SZ)]),
     "snap_compress": (_I, [_VP, _I, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
+    "snap_compress_lse": (_I, [_VP, _I, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _SZ, _VP]),
     "snap_window_logits": (_I, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP]),
     "snap_decode_append": (_I, [_VP, _VP, _I, _VP, _VP, _VP]),
     "snap_decode_attn_ws_bytes": (_I, [_P(snap_config), _I, _P(_SZ)]),
     "snap_decode_attn": (_I, [_VP, _VP, _I, _VP, _VP, _VP, _SZ, _VP]),
+    "snap_decode_step": (_I, [_VP, _VP, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "snap_check_device": (_I, [_VP, _VP]),
     "snap_decode_attn_noalloc": (_I, [_VP, _VP, _I, _VP, _VP, _VP]),
 }
@@ -207,6 +209,17 @@ class SnapCache:
                                     _ptr(Q_obs), _ptr(self.ws_compress), self.ws_compress.numel(),
                                     _stream(stream)), "snap_compress")
 
+    def compress_lse(self, slot: int, K: torch.Tensor, V: torch.Tensor | None, Q_obs: torch.Tensor,
+                     lse_obs: torch.Tensor, stream=None) -> None:
+        """snap_compress_lse: lse_obs fp32 [W][H_q], natural-log LSE of the window rows."""
+        S = K.shape[0]
+        self.ensure_compress_ws(S)
+        assert lse_obs.dtype == torch.float32 and lse_obs.is_contiguous()
+        Q_obs = Q_obs.contiguous()
+        _check(load().snap_compress_lse(self.handle, slot, _ptr(K), _ptr(V), S, K.stride(0), K.stride(1),
+                                        _ptr(Q_obs), _ptr(lse_obs), _ptr(self.ws_compress),
+                                        self.ws_compress.numel(), _stream(stream)), "snap_compress_lse")
+
     def window_logits(self, K: torch.Tensor, Q_obs: torch.Tensor, stream=None) -> torch.Tensor:
         """Base-2 logits of the observation rows against every prompt key:
         fp32 [H_kv][G*W][S] (the compression's score GEMM, for inspection)."""
@@ -236,6 +249,19 @@ class SnapCache:
         _check(load().snap_decode_attn(self.handle, _ptr(slots), n, _ptr(q.contiguous()), _ptr(out),
                                        _ptr(self.ws_decode), self.ws_decode.numel(), _stream(stream)),
                "snap_decode_attn")
+        return out
+
+    def decode_step(self, slots: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor | None,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """snap_decode_step: append k_new/v_new, then attend with q (one call)."""
+        assert slots.dtype == torch.int32 and slots.is_contiguous()
+        n = slots.numel()
+        if out is None:
+            out = torch.empty((n, self.cfg.n_q_heads, self.cfg.d_v), dtype=torch.float32, device=self.device)
+        _check(load().snap_decode_step(self.handle, _ptr(slots), n, _ptr(q.contiguous()), _ptr(k_new.contiguous()),
+                                       _ptr(v_new.contiguous() if v_new is not None else None), _ptr(out),
+                                       _ptr(self.ws_decode), self.ws_decode.numel(), _stream(stream)),
+               "snap_decode_step")
         return out
 
     def decode_attn_noalloc(self, slots: torch.Tensor, q: torch.Tensor, out: torch.Tensor,

@@ -157,6 +157,18 @@ snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void
                           void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * snap_compress() for a caller whose prefill attention already produced the
+ * log-sum-exp of the observation rows (a flash-attention kernel returns it for every
+ * query position).  lse_obs: device fp32 [W][n_q_heads], natural log of
+ * sum_j exp(sm_scale * q.k_j) over the causal row of query head i at prompt position
+ * S-W+w.  The row pass is skipped; everything else is snap_compress().  The result is
+ * the same as snap_compress() up to the rounding of the supplied LSE.
+ */
+snap_status snap_compress_lse(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
+                              int64_t tok_stride, int64_t head_stride, const void* Q_obs, const float* lse_obs,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Inspection of the compression's score GEMM: the base-2 logits
  * out[h][r][j] = log2(e) * sm_scale * q_r . k_j  (fp32 [n_kv_heads][G*W][S]) of every
  * observation row r = w*G + g (query head h*G+g at position S-W+w) against every
@@ -195,6 +207,14 @@ snap_status snap_decode_attn_ws_bytes(const snap_config* cfg, int max_n, size_t*
  */
 snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, const void* q,
                              void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * One decode step: snap_decode_append() of k_new/v_new followed by snap_decode_attn()
+ * of q, on the same stream (the form a serving loop captures into a CUDA graph).
+ * Same arguments, results and workspace as the two calls.
+ */
+snap_status snap_decode_step(snap_cache* cache, const int32_t* slots, int n, const void* q, const void* k_new,
+                             const void* v_new, void* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Synchronises `stream`, reads the device status word, clears it, and returns it

@@ -102,7 +102,7 @@ def test_compress_group_of_eight_and_strided_inputs():
 
 def test_compress_mla_small():
     """DeepSeek MLA latent layout (576-wide key row, value = first 512 columns)."""
-    wl = inputs.Workload("mla_small", 1, 32, 1, 576, 512, 4, 40, 64, 8, 5, 1, 0, 0, 0,
+    wl = inputs.Workload("mla_small", 1, 128, 1, 576, 512, 4, 40, 64, 4, 5, 1, 0, 0, 0,
                          1 / math.sqrt(192))
     pre, cache, ocache = run_compress(wl, 700, seed=11)
     check_all(wl, pre, cache, ocache, where="mla small")
@@ -122,3 +122,38 @@ def test_compress_reuses_slot_cleanly():
     v = cache.k_cache()[0].float()
     pos = ocache.slot_positions()
     assert float(v[torch.from_numpy(pos < 0)].abs().sum()) == 0.0
+
+
+def _window_lse(wl, K, Q):
+    """Natural-log LSE of every observation row over its causal keys, [W][H_q] (float64)."""
+    S = K.shape[0]
+    Kd = K.double().cuda()
+    Qd = Q.double().cuda()
+    out = torch.empty((wl.W, wl.n_q_heads), dtype=torch.float64, device="cuda")
+    for i in range(wl.n_q_heads):
+        h = i // wl.G
+        s = wl.sm_scale * (Qd[:, i, :] @ Kd[:, h, :].T)            # [W][S]
+        pos = torch.arange(S - wl.W, S, device="cuda").view(-1, 1)
+        s = s.masked_fill(torch.arange(S, device="cuda").view(1, -1) > pos, float("-inf"))
+        out[:, i] = torch.logsumexp(s, dim=1)
+    return out.float().contiguous()
+
+
+@pytest.mark.parametrize("mla", [False, True])
+def test_compress_with_supplied_lse_matches_oracle(mla):
+    """snap_compress_lse: the prefill's row log-sum-exp replaces the row pass."""
+    if mla:
+        wl = inputs.Workload("mla_small", 1, 128, 1, 576, 512, 4, 40, 64, 4, 5, 1, 0, 0, 0,
+                             1 / math.sqrt(192))
+        S = 700
+    else:
+        wl = inputs.WORKLOADS["gqa_2k_tiny"]
+        S = 2048 + 37
+    pre = inputs.gen_prefill(wl, S, seed=31)
+    cache = snap.SnapCache(snap_cfg(wl), max_batch=1, max_prompt=S)
+    lse = _window_lse(wl, pre.K, pre.Q)
+    cache.compress_lse(0, pre.K.cuda(), pre.V.cuda() if pre.V is not None else None, pre.Q.cuda(), lse)
+    torch.cuda.synchronize()
+    assert cache.check_device() == snap.SNAP_OK
+    ocache = oracle.compress(oracle_cfg(wl), pre.K, pre.V, pre.Q, want_pool=True)
+    check_all(wl, pre, cache, ocache, where="supplied lse")

@@ -39,12 +39,16 @@ class Batch:
         self.dslots = torch.tensor(self.slots, dtype=torch.int32, device="cuda")
         self.seed = seed
 
-    def step(self, t, append=True, isolated=False):
+    def step(self, t, append=True, isolated=False, fused=False):
         wl, n = self.wl, len(self.slots)
         tok = inputs.gen_decode(wl, n, step=t, seed=self.seed)
-        if append:
-            self.cache.decode_append(self.dslots, tok.k.cuda(), tok.v.cuda() if tok.v is not None else None)
-        out = self.cache.decode_attn(self.dslots, tok.q.cuda())
+        if fused:
+            out = self.cache.decode_step(self.dslots, tok.q.cuda(), tok.k.cuda(),
+                                         tok.v.cuda() if tok.v is not None else None)
+        else:
+            if append:
+                self.cache.decode_append(self.dslots, tok.k.cuda(), tok.v.cuda() if tok.v is not None else None)
+            out = self.cache.decode_attn(self.dslots, tok.q.cuda())
         torch.cuda.synchronize()
         assert self.cache.check_device() == snap.SNAP_OK
         for i in range(n):
@@ -83,6 +87,17 @@ def test_decode_continuous_batch_ring_offsets():
     for t in range(80):
         b.step(t, isolated=(t % 20 == 0))
     b.check_rows()
+
+
+def test_fused_decode_step_continuous_batch():
+    """snap_decode_step (append + attention in one launch) over a continuous batch at
+    different ring offsets, with splits (cache 4096) and without (cache 128)."""
+    for C_parts, lengths in (((4, 2044, 2048), [6000, 300, 2100, 4500]), ((4, 60, 64), [300, 37, 129, 2])):
+        wl = inputs.Workload("fused", 0, 32, 8, 128, 128, *C_parts, 16, 7, 4, 0, 0, 0, 1 / math.sqrt(128))
+        b = Batch(wl, lengths, slots=[2, 0, 3, 1], seed=17, max_batch=4)
+        for t in range(70):
+            b.step(t, fused=True, isolated=(t == 69))
+        b.check_rows()
 
 
 def test_decode_subset_of_slots():
@@ -134,13 +149,24 @@ def test_decode_compressed_equals_full_when_cache_covers():
 
 
 def test_decode_mla_small():
-    """MLA latent layout: 576-wide keys, values = first 512 columns, 32 query heads."""
-    wl = inputs.Workload("mla_small", 1, 32, 1, 576, 512, 4, 40, 64, 8, 5, 1, 0, 0, 0,
+    """MLA latent layout: 576-wide keys, values = first 512 columns, 128 query heads;
+    ragged cache (C = 4 + 40 + 100, not a multiple of the 64-key tile), one sequence
+    shorter than the cache, enough steps to wrap the ring."""
+    wl = inputs.Workload("mla_small", 1, 128, 1, 576, 512, 4, 40, 100, 4, 5, 1, 0, 0, 0,
                          1 / math.sqrt(192))
     b = Batch(wl, [700, 90], [1, 0], seed=12)
-    for t in range(70):
-        b.step(t, isolated=(t == 69))
+    for t in range(110):
+        b.step(t, isolated=(t == 109))
     b.check_rows()
+
+
+def test_decode_mla_long_cache_splits():
+    """MLA over a 4096-slot cache (many 64-key tiles, several splits, merge)."""
+    wl = inputs.Workload("mla_mid", 1, 128, 1, 576, 512, 64, 960, 3072, 8, 7, 1, 0, 0, 0,
+                         1 / math.sqrt(192))
+    b = Batch(wl, [6000, 2500, 4100], [0, 1, 2], seed=13)
+    for t in range(3):
+        b.step(t, isolated=(t == 2))
 
 
 def test_decode_out_of_range_slot_reports_without_fault():

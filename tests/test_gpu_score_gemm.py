@@ -28,7 +28,7 @@ def reference_logits(wl, K, Q):
     dict(Hq=32, Hkv=8, d=128, W=32, S=2048),      # R = 128
     dict(Hq=16, Hkv=2, d=128, W=16, S=777),       # G = 8, R = 128
     dict(Hq=32, Hkv=8, d=128, W=3, S=300),        # R = 12 (one partial row tile)
-    dict(Hq=32, Hkv=1, d=576, W=8, S=600, mla=True),   # MLA latent rows, R = 256
+    dict(Hq=128, Hkv=1, d=576, W=2, S=600, mla=True),  # MLA latent rows, R = 256
     dict(Hq=128, Hkv=1, d=576, W=3, S=450, mla=True),  # R = 384: three row tiles
 ])
 def test_window_logits_match_matmul(shape):
