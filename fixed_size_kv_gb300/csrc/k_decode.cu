@@ -254,32 +254,41 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
 // =================================================================== merge
 // out[b][i][:] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s  (zero if empty).
 // Partial index: ((b * Hkv + h) * splits + s) * G + hh  for query head i = h*G + hh.
+// One warp turns the (max, sum) pairs into weights in shared memory once; every
+// output column then reads its splits with independent loads.
 __global__ void decode_merge_kernel(DecodeArgs a) {
+    __shared__ float w_s[32];
+    __shared__ float inv_l;
     const DevConfig& c = a.cfg;
     const int i = blockIdx.x, b = blockIdx.y;
     const int h = i / c.G, hh = i % c.G;
     const int slot = a.slots[b];
     const bool ok = slot >= 0 && slot < c.max_batch;
-    float M = NEG_INF;
-    if (ok)
-        for (int s = 0; s < a.splits; ++s) {
-            const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + s) * c.G + hh;
-            M = fmaxf(M, a.part_ml[pi * 2]);
-        }
-    float L = 0.f;
-    if (M != NEG_INF)
-        for (int s = 0; s < a.splits; ++s) {
-            const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + s) * c.G + hh;
-            L += ex2(a.part_ml[pi * 2] - M) * a.part_ml[pi * 2 + 1];
-        }
+    const size_t p0 = ((size_t)b * c.Hkv + h) * a.splits;
+    if (threadIdx.x < 32) {
+        const int s = threadIdx.x;
+        const bool in = ok && s < a.splits;
+        const float m = in ? a.part_ml[((p0 + s) * c.G + hh) * 2] : NEG_INF;
+        const float l = in ? a.part_ml[((p0 + s) * c.G + hh) * 2 + 1] : 0.f;
+        float M = m;
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, x));
+        const float w = (M == NEG_INF || m == NEG_INF) ? 0.f : ex2(m - M);
+        float L = w * l;
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) L += __shfl_xor_sync(0xffffffffu, L, x);
+        w_s[s] = w;
+        if (s == 0) inv_l = L > 0.f ? 1.f / L : 0.f;
+    }
+    __syncthreads();
+    const float il = inv_l;
     for (int d = threadIdx.x; d < c.dv; d += blockDim.x) {
         float O = 0.f;
-        if (M != NEG_INF)
-            for (int s = 0; s < a.splits; ++s) {
-                const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + s) * c.G + hh;
-                O += ex2(a.part_ml[pi * 2] - M) * a.part_o[pi * c.dv + d];
-            }
-        a.out[((size_t)b * c.Hq + i) * c.dv + d] = L > 0.f ? O / L : 0.f;
+        if (il != 0.f) {
+#pragma unroll 8
+            for (int s = 0; s < a.splits; ++s) O += w_s[s] * a.part_o[((p0 + s) * c.G + hh) * c.dv + d];
+        }
+        a.out[((size_t)b * c.Hq + i) * c.dv + d] = O * il;
     }
 }
 

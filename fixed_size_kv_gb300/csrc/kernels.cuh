@@ -27,11 +27,11 @@ struct DecodeArgs {
 };
 
 constexpr int GQA_KEYS = 32;     // keys per warp step of the GQA decode kernel
-constexpr int MLA_KEYS = 64;     // keys per tile of the MLA decode kernel
+constexpr int MLA_KEYS = 32;     // keys per tile of the MLA decode kernel
 constexpr int MLA_HEADS = 128;   // query heads of the MLA layout (the M of its MMAs)
 
 cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
-// tq: queries [n][128][576], box {64, 128, 1}; tkv: cache [max_batch][C][576], box {64, 64, 1}
+// tq: queries [n][128][576], box {64, 128, 1}; tkv: cache [max_batch][C][576], box {64, 32, 1}
 cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv,
                                  cudaStream_t st);
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st);

@@ -265,7 +265,7 @@ int decode_splits(int base, int tiles, int ctas_per_sm) {
 }
 
 // Splits of one decode-attention call: enough CTAs for whole waves (GQA: 4 warps walk
-// a split, one 32-key tile each per step; MLA: two CTAs per split, 64-key tiles).
+// a split, one 32-key tile each per step; MLA: two CTAs per split, 32-key tiles).
 int decode_split_count(const snap_cache* cache, int n) {
     const snap_config& c = cache->cfg;
     if (c.layout == SNAP_LAYOUT_GQA) {
