@@ -15,17 +15,26 @@
 // weights), and each accumulates its half of O = P V in TMEM (256 fp32 columns).
 // No score is computed twice and each cache byte is read by one CTA only.
 //
-// Roles (192 threads per CTA): warp 0 issues TMA loads (and L2 prefetches ahead),
+// The A operands of both products live in TMEM: this CTA's part of Q (loaded once)
+// and the bf16 weights P of each tile (written there by the softmax), so the
+// tensor core reads only the cache tile from shared memory.  TMEM columns:
+// scores 0..63 (two 32-key buffers), P 64..95 (two 32-key buffers), Q 96..255
+// (up to 5 chunks of 64 bf16), this CTA's half of O 256..511.
+//
+// Roles (320 threads per CTA): warp 0 issues TMA loads (and L2 prefetches ahead),
 // warp 1 owns TMEM and one thread issues tcgen05.mma from two queues (scores of the
-// next tile, P V of the oldest ready tile), warps 2..5 (one TMEM lane quarter each;
-// thread = head) run the softmax.  The softmax loop is software-pipelined: the
-// TMEM load of tile i+1's partial scores is issued before tile i's exchange and max,
-// and those partials go to the peer before tile i's weights are computed, so the
-// exchange travels while the math runs.  Exchange buffers and the weight buffer P
-// are double-buffered (P's two tiles share each 128-byte swizzled row), so the
-// weights of tile i are written while P V of tile i-1 still runs.
-// The running max is updated lazily (only when a tile's max exceeds it by more than
-// 32 in log2 units), so O in TMEM is rescaled rarely.  Every wait is bounded.
+// next tile, P V of the oldest ready tile).  Warps 2..9 run the softmax as two
+// groups of four warps (one TMEM lane quarter each; thread = head) that take
+// alternate tiles, so two tiles are in the softmax at once: while one group waits
+// for the peer's partial scores, the other computes weights.  Each group has its
+// own score buffer, exchange buffers and weight buffer.
+//
+// Both groups accumulate into the one O in TMEM, so they share one running max.
+// It is handed from the group of tile i-1 to the group of tile i (per lane
+// quarter, through an mbarrier) and moves lazily: only when a tile's max exceeds it
+// by more than 32 in log2 units, and then O is rescaled in TMEM after P V of the
+// previous tile.  Each group keeps its own sum of weights, rescaled whenever the
+// shared max moves; the two sums are added at the end.  Every wait is bounded.
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -38,40 +47,45 @@ constexpr int MV = 512;                     // value (latent) width
 constexpr int HEADS = 128;                  // M of every MMA
 constexpr int TK = 32;                      // keys per tile
 constexpr int CH_B = TK * 128;              // one 64-column chunk of a KV tile: 4 KB
-constexpr int QCH_B = HEADS * 128;          // one 64-column chunk of Q: 16 KB
 constexpr int MAXCH = 5;                    // chunks owned by rank 1
-constexpr int KST = 4;                      // KV tile stages
-constexpr int THREADS = 192;
+constexpr int KST = 6;                      // KV tile stages
+constexpr int NG = 2;                       // softmax groups (tile i goes to group i % 2)
+constexpr int THREADS = 64 + NG * 128;
 constexpr float RESCALE_GAP = 32.f;         // weights up to 2^32 stay exact in fp32 O and l
 constexpr int XROW_B = TK * 4;              // one head's partial scores: 128 B
+constexpr int XBUF_B = HEADS * XROW_B;      // one tile's partial scores: 16 KB
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + MAXCH * QCH_B;             // 80 KB
-constexpr int OFF_P = OFF_KV + KST * MAXCH * CH_B;        // + 80 KB
-constexpr int OFF_X = OFF_P + HEADS * 128;                // + 16 KB (P: 128-byte rows, two 32-key tiles)
-constexpr int OFF_BAR = OFF_X + 2 * HEADS * XROW_B;       // + 32 KB (two exchange buffers)
+constexpr int OFF_KV = 0;
+constexpr int OFF_X = OFF_KV + KST * MAXCH * CH_B;        // 120 KB
+constexpr int OFF_XS = OFF_X + NG * XBUF_B;               // + 32 KB (incoming partial scores, per group)
+constexpr int OFF_ML = OFF_XS + NG * XBUF_B;              // + 32 KB (outgoing partial scores, per group)
+constexpr int OFF_BAR = OFF_ML + 2048;                    // + running max [128] and group sums [2][128]
 constexpr int SMEM = OFF_BAR + 256 + 1024;                // barriers + alignment slack
 
 enum {
     B_Q_FULL = 0,
     B_KV_FULL = 1,               // + KST
     B_KV_EMPTY = 1 + KST,        // + KST
-    B_S_FULL = 1 + 2 * KST,      // + 2
-    B_S_EMPTY = 3 + 2 * KST,     // + 2
-    B_P_FULL = 5 + 2 * KST,      // + 2
-    B_P_EMPTY = 7 + 2 * KST,     // + 2
-    B_X_FULL = 9 + 2 * KST,      // + 2
-    B_X_EMPTY = 11 + 2 * KST,    // + 2
-    N_BARS = 13 + 2 * KST
+    B_S_FULL = 1 + 2 * KST,      // + NG
+    B_S_EMPTY = 3 + 2 * KST,     // + NG
+    B_P_FULL = 5 + 2 * KST,      // + NG
+    B_P_EMPTY = 7 + 2 * KST,     // + NG
+    B_X_FULL = 9 + 2 * KST,      // + NG
+    B_X_EMPTY = 11 + 2 * KST,    // + NG
+    B_M_READY = 13 + 2 * KST,    // + 4 (one per lane quarter)
+    N_BARS = 17 + 2 * KST
 };
+static_assert((N_BARS + 1) * 8 <= 256, "barrier area");
+static_assert(SMEM <= 232448, "shared memory");
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, bool cluster) {
-    return mbar_wait_bounded(bar, parity, abort_flag, cluster);
+constexpr int SOFTMAX_BAR_ID = 1;           // named barrier of the softmax warps (bar 0 = __syncthreads)
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    return mbar_wait_bounded(bar, parity, abort_flag);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
-    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
-                         DecodeArgs a) {
+    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV, DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const DevConfig& c = a.cfg;
@@ -83,29 +97,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int c0 = rank == 0 ? 0 : 4;           // first owned chunk
 
     const uint32_t s_base = smem_u32(smem);
-    const uint32_t s_q = s_base + OFF_Q, s_kv = s_base + OFF_KV, s_p = s_base + OFF_P, s_x = s_base + OFF_X;
+    const uint32_t s_kv = s_base + OFF_KV, s_x = s_base + OFF_X;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     auto bar = [&](int i) { return smem_u32(bars + i); };
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + N_BARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    float* m_sh = reinterpret_cast<float*>(smem + OFF_ML);         // running max handed between groups
+    float* l_sh = m_sh + HEADS;                                    // [NG][HEADS] group sums at the end
 
     const int slot = a.slots[b];
     const bool slot_ok = slot >= 0 && slot < c.max_batch;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(B_Q_FULL), 1);
+        mbar_init(bar(B_Q_FULL), NG * 4);      // the softmax warps, after storing Q into TMEM
         for (int i = 0; i < KST; ++i) {
             mbar_init(bar(B_KV_FULL + i), 1);
             mbar_init(bar(B_KV_EMPTY + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_S_FULL + i), 1);
-            mbar_init(bar(B_S_EMPTY + i), 4);
-            mbar_init(bar(B_X_FULL + i), 1);    // this CTA's expect_tx + the peer's st.async bytes
-            mbar_init(bar(B_X_EMPTY + i), 4);   // the peer's four softmax warps
-            mbar_init(bar(B_P_FULL + i), 4);
-            mbar_init(bar(B_P_EMPTY + i), 1);
+        for (int g = 0; g < NG; ++g) {
+            mbar_init(bar(B_S_FULL + g), 1);
+            mbar_init(bar(B_S_EMPTY + g), 4);
+            mbar_init(bar(B_X_FULL + g), 1);    // this CTA's expect_tx + the peer's bulk-copy bytes
+            mbar_init(bar(B_X_EMPTY + g), 4);   // the peer's four warps of group g
+            mbar_init(bar(B_P_FULL + g), 4);
+            mbar_init(bar(B_P_EMPTY + g), 1);
         }
+        for (int q = 0; q < 4; ++q) mbar_init(bar(B_M_READY + q), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -117,8 +134,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     cluster_sync_all();                 // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    // TMEM: scores (two buffers) at columns 0 and 32; this CTA's half of O at 256..511
-    const uint32_t T_S = tmem, T_O = tmem + 256;
+    // TMEM: scores (one 32-column buffer per group), P (one 16-column buffer per group), Q, O
+    const uint32_t T_S = tmem, T_P = tmem + 64, T_Q = tmem + 96, T_O = tmem + 256;
 
     // status detail: 300 + rank, the wait that gave up, the tile index reached
     int cur_tile = -1;
@@ -146,10 +163,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && t_begin < t_end) {
-            tma_prefetch(&tmQ);
             tma_prefetch(&tmKV);
-            mbar_expect_tx(bar(B_Q_FULL), nch * QCH_B);
-            for (int j = 0; j < nch; ++j) tma_load_3d(s_q + j * QCH_B, &tmQ, bar(B_Q_FULL), 64 * (c0 + j), 0, b);
             constexpr int AHEAD = 8;    // tiles on their way to L2 ahead of the loads
             for (int t = t_begin; t < min(t_end, t_begin + AHEAD); ++t)
                 for (int j = 0; j < nch; ++j) tma_prefetch_3d(&tmKV, 64 * (c0 + j), t * TK, slot);
@@ -160,7 +174,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     for (int j = 0; j < nch; ++j) tma_prefetch_3d(&tmKV, 64 * (c0 + j), (t + AHEAD) * TK, slot);
                 const int st = i % KST;
                 const uint32_t n = i / KST;
-                if (!wait_bar(bar(B_KV_EMPTY + st), (n & 1) ^ 1, abort_flag, false)) { fail(0); break; }
+                if (!wait_bar(bar(B_KV_EMPTY + st), (n & 1) ^ 1, abort_flag)) { fail(0); break; }
                 mbar_expect_tx(bar(B_KV_FULL + st), nch * CH_B);
                 for (int j = 0; j < nch; ++j)
                     tma_load_3d(s_kv + (st * MAXCH + j) * CH_B, &tmKV, bar(B_KV_FULL + st), 64 * (c0 + j), t * TK,
@@ -171,8 +185,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && t_begin < t_end) {
             const uint32_t id_qk = idesc_bf16(HEADS, TK);
-            const uint32_t id_pv = idesc_bf16_bmn(HEADS, 64);
-            bool ok = wait_bar(bar(B_Q_FULL), 0, abort_flag, false);
+            const uint32_t id_pv = idesc_bf16_bmn(HEADS, 256);   // all four value chunks per MMA
+            bool ok = wait_bar(bar(B_Q_FULL), 0, abort_flag);
             if (!ok) fail(10);
             // Two queues: the scores of the next tile (needs its KV and a free score
             // buffer) and P V of the oldest tile with weights ready.  Issue whichever is
@@ -189,9 +203,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     const int st = qk % KST, sb = qk & 1;
                     for (int j = 0; j < nch; ++j)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc_mma(T_S + sb * TK, desc_sw128(s_q + j * QCH_B + k * 32),
-                                   desc_sw128(s_kv + (st * MAXCH + j) * CH_B + k * 32), id_qk, (j | k) ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k)     // 16 columns (8 TMEM columns of Q) per step
+                            tc_mma_ta(T_S + sb * TK, T_Q + j * 32 + k * 8,
+                                      desc_sw128(s_kv + (st * MAXCH + j) * CH_B + k * 32), id_qk, (j | k) ? 1u : 0u);
                     tc_commit(bar(B_S_FULL + sb));
                     ++qk;
                     progressed = true;
@@ -199,14 +213,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (pv < qk && mbar_test_wait(bar(B_P_FULL + (pv & 1)), (pv >> 1) & 1)) {
                     tc_fence_after();
                     const int stp = pv % KST;
-                    const uint32_t pa = s_p + (pv & 1) * 64;   // this tile's half of the P rows
+                    const uint32_t pa = T_P + (pv & 1) * (TK / 2);  // this tile's weights
+                    // N = 256: this CTA's four 64-column value chunks (CH_B apart) in one MMA
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)             // this CTA's four value chunks
-#pragma unroll
-                        for (int k = 0; k < TK / 16; ++k)   // 16 keys per step
-                            tc_mma(T_O + j * 64, desc_sw128(pa + k * 32),
-                                   desc_sw128_mn(s_kv + (stp * MAXCH + j) * CH_B + k * 2048), id_pv,
-                                   (pv > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < TK / 16; ++k)       // 16 keys (8 TMEM columns of P) per step
+                        tc_mma_ta(T_O, pa + k * 8, desc_sw128_mn(s_kv + stp * MAXCH * CH_B + k * 2048, CH_B), id_pv,
+                                  (pv > 0 || k > 0) ? 1u : 0u);
                     tc_commit(bar(B_P_EMPTY + (pv & 1)));
                     tc_commit(bar(B_KV_EMPTY + stp));
                     ++pv;
@@ -224,79 +236,104 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ softmax warps
-        const int quarter = warp & 3;
+        // ------------------------------------------------------------ softmax groups
+        const int g = (warp - 2) >> 2;          // group: takes the tiles i with i % NG == g
+        const int quarter = warp & 3;           // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;    // query head
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = c.scale_log2;
-        int n_t = 0;
-        for (int t = next_tile(t_begin); t < t_end; t = next_tile(t + 1)) ++n_t;
+        const uint32_t s_xs_warp = s_base + OFF_XS + g * XBUF_B + quarter * 32 * XROW_B;
+        const uint32_t m_ready = bar(B_M_READY + quarter);
         bool ok = true;
+
+        // This CTA's columns of q (64-column chunks c0 .. c0+nch-1) into TMEM, one
+        // head per lane; the two groups take alternate chunks.
+        {
+            const bf16* qrow = a.q + ((size_t)b * c.Hq + row) * (size_t)c.dqk + 64 * c0;
+            for (int j = g; j < nch; j += NG) {
+                const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * j);
+                float v[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint4 u = src[e];
+                    v[4 * e] = __uint_as_float(u.x);
+                    v[4 * e + 1] = __uint_as_float(u.y);
+                    v[4 * e + 2] = __uint_as_float(u.z);
+                    v[4 * e + 3] = __uint_as_float(u.w);
+                }
+                tmem_st32(T_Q + lane_off + 32 * j, v);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_Q_FULL));
+        }
+
         // Sends tile j's partial scores (in registers) into the peer's exchange buffer
-        // j & 1; the 16-byte chunks of a 128-byte row are XOR-swizzled by row so that a
-        // warp reading chunk k of 32 rows hits distinct banks.
+        // of this group: the warp stages its 32 rows in shared memory and one lane
+        // hands the 4 KB to the TMA engine as one bulk copy into the peer.  The 16-byte
+        // chunks of a 128-byte row are XOR-swizzled by row so that a warp reading or
+        // writing chunk k of 32 rows hits distinct banks.
         auto send = [&](int j, const float (&s)[TK]) -> bool {
-            const int xb = j & 1;
-            // the peer has consumed what this CTA sent two tiles ago into that buffer
-            if (!__all_sync(0xffffffffu, wait_bar(bar(B_X_EMPTY + xb), ((j >> 1) & 1) ^ 1, abort_flag, true)))
-                return false;
-            // the peer's scores of tile j will land in this CTA's buffer xb: announce the bytes
-            if (quarter == 0 && lane == 0) mbar_expect_tx(bar(B_X_FULL + xb), HEADS * XROW_B);
-            const uint32_t dst = mapa(s_x + xb * HEADS * XROW_B + row * XROW_B, peer);
-            const uint32_t xfull_peer = mapa(bar(B_X_FULL + xb), peer);
+            // the bulk copy of this group's previous tile has finished reading the staging rows
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            const uint32_t srow = s_xs_warp + lane * XROW_B;
 #pragma unroll
             for (int k = 0; k < TK / 4; ++k)
-                st_async_v4(dst + 16 * (k ^ (row & 7)), s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3], xfull_peer);
-            return true;
+                asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + 16 * (k ^ (row & 7))),
+                             "f"(s[4 * k]), "f"(s[4 * k + 1]), "f"(s[4 * k + 2]), "f"(s[4 * k + 3])
+                             : "memory");
+            fence_proxy_async();
+            // the peer's scores of tile j will land in this group's buffer: announce the bytes
+            if (quarter == 0 && lane == 0) mbar_expect_tx(bar(B_X_FULL + g), XBUF_B);
+            __syncwarp();
+            bool ok_send = true;
+            if (lane == 0) {
+                // the peer has consumed what this group sent for its previous tile
+                ok_send = wait_bar(bar(B_X_EMPTY + g), ((j >> 1) & 1) ^ 1, abort_flag);
+                if (ok_send) {
+                    bulk_copy_to_cluster(mapa(s_x + g * XBUF_B + quarter * 32 * XROW_B, peer), s_xs_warp,
+                                         32 * XROW_B, mapa(bar(B_X_FULL + g), peer));
+                    bulk_commit();
+                }
+            }
+            return __shfl_sync(0xffffffffu, ok_send, 0);
         };
-        // Issues the TMEM load of tile j's partial scores (completed by finish_scores).
-        auto start_scores = [&](int j, float (&s)[TK]) -> bool {
-            const int sb = j & 1;
-            if (!__all_sync(0xffffffffu, wait_bar(bar(B_S_FULL + sb), (j >> 1) & 1, abort_flag, false))) return false;
+
+        float m_used = NEG_INF;     // the running max this group's sum l_g is relative to
+        float l_g = 0.f;
+        int i = 0;
+        for (int t = next_tile(t_begin); t < t_end; t = next_tile(t + 1), ++i) {
+            if ((i & 1) != g || !ok) continue;
+            cur_tile = t;
+            const int k_g = i >> 1;             // this group's k-th tile: barrier phase parity k_g & 1
+            // 1. this CTA's partial scores of tile i, out of TMEM
+            float s[TK];
+            if (!__all_sync(0xffffffffu, wait_bar(bar(B_S_FULL + g), k_g & 1, abort_flag))) {
+                fail(3);
+                ok = false;
+                continue;
+            }
             tc_fence_after();
-            tmem_ld32(T_S + lane_off + sb * TK, s);
-            return true;
-        };
-        // Waits for that load and frees the score buffer for the scores of tile j + 2.
-        auto finish_scores = [&](int j, float (&s)[TK]) {
+            tmem_ld32(T_S + lane_off + g * TK, s);
             tmem_ld_wait(s);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_S_EMPTY + (j & 1)));
-        };
-
-        float m_run = NEG_INF, l_run = 0.f;
-        float s_next[TK];
-        if (n_t > 0) {
-            if (start_scores(0, s_next)) {
-                finish_scores(0, s_next);
-                if (!send(0, s_next)) ok = false;
-            } else {
+            if (lane == 0) mbar_arrive(bar(B_S_EMPTY + g));
+            // 2. to the peer
+            if (!send(i, s)) {
+                fail(6);
                 ok = false;
+                continue;
             }
-            if (!ok) fail(2);
-        }
-        int i = 0;
-        for (int t = next_tile(t_begin); ok && t < t_end; t = next_tile(t + 1), ++i) {
-            cur_tile = t;
-            float s[TK];
-#pragma unroll
-            for (int k = 0; k < TK; ++k) s[k] = s_next[k];
-            // 1. the TMEM load of the next tile's partial scores runs during steps 2-3
-            const bool has_next = i + 1 < n_t;
-            if (has_next && !start_scores(i + 1, s_next)) {
-                fail(3);
-                ok = false;
-                break;
-            }
-            // 2. the peer's partial scores of this tile
-            const int xb = i & 1;
-            if (!__all_sync(0xffffffffu, wait_bar(bar(B_X_FULL + xb), (i >> 1) & 1, abort_flag, true))) {
+            // 3. the peer's partial scores of this tile
+            if (!__all_sync(0xffffffffu, wait_bar(bar(B_X_FULL + g), k_g & 1, abort_flag))) {
                 fail(4);
                 ok = false;
-                break;
+                continue;
             }
-            const float4* xr = reinterpret_cast<const float4*>(smem + OFF_X + xb * HEADS * XROW_B + row * XROW_B);
+            const float4* xr = reinterpret_cast<const float4*>(smem + OFF_X + g * XBUF_B + row * XROW_B);
 #pragma unroll
             for (int k = 0; k < TK / 4; ++k) {
                 const float4 v = xr[k ^ (row & 7)];
@@ -307,8 +344,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 s[4 * k + 3] += v.w;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa(bar(B_X_EMPTY + xb), peer));
-            // 3. mask (one ballot for the tile's 32 slots), scale, tile max
+            if (lane == 0) mbar_arrive_remote(mapa(bar(B_X_EMPTY + g), peer));
+            // 4. mask (one ballot for the tile's 32 slots), scale, tile max
             const uint32_t vmask = __ballot_sync(0xffffffffu, t * TK + lane < c.C && sv.valid(t * TK + lane));
             float mt = NEG_INF;
 #pragma unroll
@@ -316,33 +353,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 s[k] = ((vmask >> k) & 1u) ? s[k] * sl2 : NEG_INF;
                 mt = fmaxf(mt, s[k]);
             }
-            // 4. the next tile's partial scores go to the peer before this tile's weights
-            if (has_next) {
-                finish_scores(i + 1, s_next);
-                if (!send(i + 1, s_next)) {
-                    fail(6);
+            // 5. the running max as left by tile i-1 (the other group)
+            float m_prev = NEG_INF;
+            if (i > 0) {
+                if (!__all_sync(0xffffffffu, wait_bar(m_ready, (i - 1) & 1, abort_flag))) {
+                    fail(9);
                     ok = false;
-                    break;
+                    continue;
                 }
+                m_prev = m_sh[row];
             }
-            // 5. lazy max: each lane (head) decides whether its max moved; the TMEM
-            //    rescale of O is done by the whole warp (tcgen05.ld/st are
-            //    warp-collective), with factor 1 on the lanes whose max stays, once P V
-            //    of tile i-1 (the last one issued) is complete.
-            const bool move = mt > m_run + RESCALE_GAP || (m_run == NEG_INF && mt != NEG_INF);
-            const float m_new = move ? fmaxf(mt, m_run) : m_run;
-            const bool rescale_lane = move && m_run != NEG_INF;
+            // lazy max: each lane (head) decides whether its max moves; the TMEM rescale
+            // of O is done by the whole warp (tcgen05.ld/st are warp-collective), with
+            // factor 1 on the lanes whose max stays, once P V of tile i-1 is complete
+            // (P V of tile i is not issued before this tile's weights exist).
+            const bool move = mt > m_prev + RESCALE_GAP || (m_prev == NEG_INF && mt != NEG_INF);
+            const float m_new = move ? fmaxf(mt, m_prev) : m_prev;
+            const bool rescale_lane = move && m_prev != NEG_INF;
             if (__any_sync(0xffffffffu, rescale_lane)) {
-                // a lane with a finite running max had weights in an earlier tile: i >= 1
+                // a lane with a finite running max saw weights in an earlier tile: i >= 1
                 if (!__all_sync(0xffffffffu,
-                                wait_bar(bar(B_P_EMPTY + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag, false))) {
+                                wait_bar(bar(B_P_EMPTY + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag))) {
                     fail(5);
                     ok = false;
-                    break;
+                    continue;
                 }
                 tc_fence_after();
-                const float alpha = rescale_lane ? ex2(m_run - m_new) : 1.f;
-                l_run *= alpha;
+                const float alpha = rescale_lane ? ex2(m_prev - m_new) : 1.f;
 #pragma unroll 1
                 for (int j = 0; j < 8; ++j) {
                     float o[32];
@@ -355,53 +392,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 tmem_st_wait();
                 tc_fence_before();
             }
-            m_run = m_new;
-            // 6. weights (bf16) into this tile's half of the P rows (128-byte swizzled
-            //    K-major rows: tile i uses 16-byte chunks 4 (i & 1) .. 4 (i & 1) + 3),
-            //    once P V of tile i-2 has released that half
-            if (!__all_sync(0xffffffffu, wait_bar(bar(B_P_EMPTY + (i & 1)), ((i >> 1) & 1) ^ 1, abort_flag, false))) {
+            // 6. this group's half of P is free once P V of its previous tile is done
+            if (!__all_sync(0xffffffffu, wait_bar(bar(B_P_EMPTY + g), (k_g & 1) ^ 1, abort_flag))) {
                 fail(7);
                 ok = false;
-                break;
+                continue;
             }
-            const uint32_t prow = s_p + (row >> 3) * 1024 + (row & 7) * 128;
+            // 7. hand the running max to tile i+1 (after the wait above, so that the
+            //    other group's waits on this group's P barrier see its current phase)
+            m_sh[row] = m_new;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(m_ready);
+            if (m_used != m_new) {
+                l_g = m_used == NEG_INF ? l_g : l_g * ex2(m_used - m_new);
+                m_used = m_new;
+            }
+            // 8. weights (bf16, two keys per TMEM column) into this group's P buffer
+            uint32_t w[TK / 2];
             float psum = 0.f;
 #pragma unroll
-            for (int ch = 0; ch < TK / 8; ++ch) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = m_run == NEG_INF ? 0.f : bf16_round(ex2(s[ch * 8 + 2 * e] - m_run));
-                    const float p1 = m_run == NEG_INF ? 0.f : bf16_round(ex2(s[ch * 8 + 2 * e + 1] - m_run));
-                    psum += p0 + p1;
-                    w[e] = pack_bf16(p0, p1);
-                }
-                const uint32_t dst = prow + ((((i & 1) * 4 + ch) ^ (row & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                             "r"(w[3])
-                             : "memory");
+            for (int e = 0; e < TK / 2; ++e) {
+                const float p0 = m_new == NEG_INF ? 0.f : bf16_round(ex2(s[2 * e] - m_new));
+                const float p1 = m_new == NEG_INF ? 0.f : bf16_round(ex2(s[2 * e + 1] - m_new));
+                psum += p0 + p1;
+                w[e] = pack_bf16(p0, p1);
             }
-            l_run += psum;
-            fence_proxy_async();
+            tmem_st16(T_P + lane_off + g * (TK / 2), w);
+            tmem_st_wait();
+            tc_fence_before();
+            l_g += psum;
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL + (i & 1)));
+            if (lane == 0) mbar_arrive(bar(B_P_FULL + g));
         }
-        // 6. this CTA's half of the output (once P V of the last tile is done)
-        if (ok && i >= 1) {
-            // the commit after P V of the last tile covers every earlier MMA too
-            if (!__all_sync(0xffffffffu,
-                            wait_bar(bar(B_P_EMPTY + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag, false))) {
+        const int n_t = i;
+
+        // 9. the final running max (from the group of the last tile) and P V of the
+        //    last tile done (its commit covers every earlier MMA too)
+        float m_fin = NEG_INF;
+        if (ok && n_t > 0) {
+            if (((n_t - 1) & 1) != g &&
+                !__all_sync(0xffffffffu, wait_bar(m_ready, (n_t - 1) & 1, abort_flag))) {
                 fail(8);
                 ok = false;
             }
+            if (ok && !__all_sync(0xffffffffu, wait_bar(bar(B_P_EMPTY + ((n_t - 1) & 1)), ((n_t - 1) >> 1) & 1,
+                                                        abort_flag))) {
+                fail(8);
+                ok = false;
+            }
+            if (ok) m_fin = m_sh[row];
             tc_fence_after();
         }
+        if (l_g > 0.f && m_used != m_fin) l_g = m_fin == NEG_INF ? 0.f : l_g * ex2(m_used - m_fin);
+        l_sh[g * HEADS + row] = l_g;
+        asm volatile("bar.sync %0, %1;\n" ::"n"(SOFTMAX_BAR_ID), "n"(NG * 128) : "memory");
+        const float l_run = l_sh[row] + l_sh[HEADS + row];
+
+        // 10. this CTA's half of the output; group g writes TMEM columns 128 g .. 128 g + 127
         if (ok && row < c.Hq) {
             const int head = row;
             const int d0 = rank == 0 ? 0 : 256;
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 4 * g; j < 4 * g + 4; ++j) {
                 float o[32];
-                if (i >= 1) {
+                if (n_t > 0) {
                     tmem_ld32(T_O + lane_off + j * 32, o);
                     tmem_ld_wait();
                 } else {
@@ -422,12 +475,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     *reinterpret_cast<float4*>(dst + e) =
                         make_float4(o[e] * scale, o[e + 1] * scale, o[e + 2] * scale, o[e + 3] * scale);
             }
-            if (a.splits > 1 && rank == 0) {
+            if (a.splits > 1 && rank == 0 && g == 0) {
                 const size_t pi = ((size_t)b * a.splits + split) * c.Hq + head;
-                a.part_ml[pi * 2 + 0] = m_run;
+                a.part_ml[pi * 2 + 0] = m_fin;
                 a.part_ml[pi * 2 + 1] = l_run;
             }
         }
+        if (lane == 0) bulk_wait_read_all();    // the staging rows stay until their last copy has read them
     }
 
     __syncthreads();
@@ -440,7 +494,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
-cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv, cudaStream_t st) {
+int mla_decode_wave_ctas() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    if (cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, (const void*)mla_decode_tc_kernel, &cfg) != cudaSuccess ||
+        clusters <= 0)
+        return 0;
+    if (dev >= 0 && dev < 64) cached[dev] = 2 * clusters;
+    return 2 * clusters;
+}
+
+cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cudaStream_t st) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
@@ -448,7 +521,7 @@ cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tq, con
         attr = true;
     }
     dim3 grid(2 * a.splits, a.n);
-    mla_decode_tc_kernel<<<grid, THREADS, SMEM, st>>>(tq, tkv, a);
+    mla_decode_tc_kernel<<<grid, THREADS, SMEM, st>>>(tkv, a);
     return cudaGetLastError();
 }
 

@@ -53,7 +53,7 @@ struct Layout {
 };
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    return mbar_wait_bounded(bar, parity, abort_flag, false);
+    return mbar_wait_bounded(bar, parity, abort_flag);
 }
 
 // sum_i 2^(v_i * a + b) over 32 values, with independent partial sums

@@ -31,9 +31,11 @@ constexpr int MLA_KEYS = 32;     // keys per tile of the MLA decode kernel
 constexpr int MLA_HEADS = 128;   // query heads of the MLA layout (the M of its MMAs)
 
 cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
-// tq: queries [n][128][576], box {64, 128, 1}; tkv: cache [max_batch][C][576], box {64, 32, 1}
-cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tq, const CUtensorMap& tkv,
-                                 cudaStream_t st);
+// tkv: cache [max_batch][C][576], box {64, 32, 1} (queries are read from a.q directly)
+cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cudaStream_t st);
+// CTAs of the MLA decode kernel that can be resident at once on the current device
+// (two per co-resident cluster; 0 if the occupancy query fails).
+int mla_decode_wave_ctas();
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st);
 
 // ----------------------------------------------------------------- append

@@ -203,9 +203,8 @@ cudaError_t run_rowstat(int mode, const snap_config& c, ScoreParams sp, const vo
     return launch_score_tc(mode, tx, ty, sp, c.d_qk, true, true, num_sms(), st);
 }
 
-// MLA decode tensor maps: queries [n][128][576] (box 64 x 128) and the cache rows
-// [max_batch][C][576] (box 64 x 64).
-bool mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int n, const snap_cache* cache);
+// MLA decode tensor map of the cache rows [max_batch][C][576] (box 64 x 32).
+bool mla_cache_map(CUtensorMap* tkv, const snap_cache* cache);
 
 // Split count and launches of one decode-attention call (shared by the entry points).
 cudaError_t run_decode(snap_cache* cache, DecodeArgs& a, cudaStream_t st);
@@ -243,10 +242,9 @@ snap_status cuda_status(cudaError_t e) {
     return SNAP_ERR_CUDA;
 }
 
-// Split count for decode: enough CTAs for several full waves, never more splits
-// than tiles, and each split at least 4 tiles.
-int decode_splits(int base, int tiles, int ctas_per_sm) {
-    const int wave = num_sms() * ctas_per_sm;
+// Split count for decode: enough CTAs for whole waves of `wave` resident CTAs, never
+// more splits than tiles, and each split at least 4 tiles.
+int decode_splits(int base, int tiles, int wave) {
     int best = 1;
     double best_eff = 0.0;
     for (int s = 1; s <= MAX_DECODE_SPLITS; ++s) {
@@ -264,33 +262,43 @@ int decode_splits(int base, int tiles, int ctas_per_sm) {
     return best;
 }
 
+// CTAs of one decode-attention kernel resident at once: one per SM for GQA; for MLA
+// two per co-resident cluster (the GPCs may leave SMs that cannot host a pair).
+int decode_wave_ctas(const snap_cache* cache) {
+    if (cache->cfg.layout == SNAP_LAYOUT_GQA) return num_sms();
+    const int w = mla_decode_wave_ctas();
+    return w > 0 ? w : num_sms();
+}
+
 // Splits of one decode-attention call: enough CTAs for whole waves (GQA: 4 warps walk
 // a split, one 32-key tile each per step; MLA: two CTAs per split, 32-key tiles).
 int decode_split_count(const snap_cache* cache, int n) {
     const snap_config& c = cache->cfg;
     if (c.layout == SNAP_LAYOUT_GQA) {
         const int tiles = (int)((cache->C + GQA_KEYS - 1) / GQA_KEYS);
-        return decode_splits(n * c.n_kv_heads, tiles / 4, 1);
+        return decode_splits(n * c.n_kv_heads, tiles / 4, decode_wave_ctas(cache));
     }
     const int tiles = (int)((cache->C + MLA_KEYS - 1) / MLA_KEYS);
-    return decode_splits(2 * n, tiles, 1);
+    return decode_splits(2 * n, tiles, decode_wave_ctas(cache));
 }
 
-int decode_tiles_per_split(const snap_cache* cache, int splits) {
+// Splits and key tiles per split of one decode-attention call: the split count is
+// recomputed from the rounded-up tiles per split, so that no split is empty.
+void decode_plan(const snap_cache* cache, int n, int* splits, int* tiles_per_split) {
     const int key_tile = cache->cfg.layout == SNAP_LAYOUT_GQA ? GQA_KEYS : MLA_KEYS;
     const int tiles = (int)((cache->C + key_tile - 1) / key_tile);
-    return (tiles + splits - 1) / splits;
+    const int s = decode_split_count(cache, n);
+    const int per = (tiles + s - 1) / s;
+    *tiles_per_split = per;
+    *splits = (tiles + per - 1) / per;
 }
 
-bool mla_maps(CUtensorMap* tq, CUtensorMap* tkv, const void* q, int n, const snap_cache* cache) {
+bool mla_cache_map(CUtensorMap* tkv, const snap_cache* cache) {
     const snap_config& c = cache->cfg;
-    const cuuint64_t qd[3] = {(cuuint64_t)c.d_qk, (cuuint64_t)c.n_q_heads, (cuuint64_t)n};
-    const cuuint64_t qs[2] = {(cuuint64_t)c.d_qk * 2, (cuuint64_t)c.n_q_heads * c.d_qk * 2};
-    const cuuint32_t qb[3] = {64, (cuuint32_t)MLA_HEADS, 1};
     const cuuint64_t kd[3] = {(cuuint64_t)c.d_qk, (cuuint64_t)cache->C, (cuuint64_t)cache->max_batch};
     const cuuint64_t ks[2] = {(cuuint64_t)c.d_qk * 2, (cuuint64_t)cache->C * c.d_qk * 2};
     const cuuint32_t kb[3] = {64, (cuuint32_t)MLA_KEYS, 1};
-    return encode(tq, q, 3, qd, qs, qb) && encode(tkv, cache->k, 3, kd, ks, kb);
+    return encode(tkv, cache->k, 3, kd, ks, kb);
 }
 
 cudaError_t run_decode(snap_cache* cache, DecodeArgs& a, cudaStream_t st) {
@@ -298,9 +306,9 @@ cudaError_t run_decode(snap_cache* cache, DecodeArgs& a, cudaStream_t st) {
     if (cache->cfg.layout == SNAP_LAYOUT_GQA) {
         e = launch_decode_gqa(a, st);
     } else {
-        CUtensorMap tq, tkv;
-        if (!mla_maps(&tq, &tkv, a.q, a.n, cache)) return cudaErrorInvalidValue;
-        e = launch_decode_mla_tc(a, tq, tkv, st);
+        CUtensorMap tkv;
+        if (!mla_cache_map(&tkv, cache)) return cudaErrorInvalidValue;
+        e = launch_decode_mla_tc(a, tkv, st);
     }
     if (e == cudaSuccess && a.splits > 1) e = launch_decode_merge(a, st);
     return e;
@@ -551,6 +559,16 @@ snap_status snap_decode_attn_ws_bytes(const snap_config* cfg, int max_n, size_t*
     return SNAP_OK;
 }
 
+snap_status snap_decode_attn_plan(const snap_cache* cache, int n, int* splits, int* tiles_per_split,
+                                  int* ctas_per_wave) {
+    if (!cache || n < 1 || !splits || !tiles_per_split || !ctas_per_wave) return SNAP_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SNAP_ERR_CUDA;
+    decode_plan(cache, n, splits, tiles_per_split);
+    *ctas_per_wave = decode_wave_ctas(cache);
+    return SNAP_OK;
+}
+
 snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, const void* q,
                              void* out, void* ws, size_t ws_bytes, void* stream) {
     if (!cache || n < 0) return SNAP_ERR_INVALID_ARG;
@@ -569,9 +587,9 @@ snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, con
     a.out = static_cast<float*>(out);
     a.status = cache->status;
     a.cfg = dev_config(c, cache->max_batch);
-    const int splits = decode_split_count(cache, n);
+    int splits = 1;
+    decode_plan(cache, n, &splits, &a.tiles_per_split);
     a.splits = splits;
-    a.tiles_per_split = decode_tiles_per_split(cache, splits);
     if (splits > 1) {
         const size_t need = decode_ws_bytes(c, n);
         if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SNAP_ERR_INVALID_ARG;
@@ -661,9 +679,9 @@ extern "C" snap_status snap_decode_attn_noalloc(snap_cache* cache, const int32_t
     a.out = static_cast<float*>(out);
     a.status = cache->status;
     a.cfg = dev_config(c, cache->max_batch);
-    const int splits = decode_split_count(cache, n);
+    int splits = 1;
+    decode_plan(cache, n, &splits, &a.tiles_per_split);
     a.splits = splits;
-    a.tiles_per_split = decode_tiles_per_split(cache, splits);
     if (splits > 1) {
         // compact partial layout for this call: O then (max, sum)
         const size_t parts = (size_t)n * c.n_q_heads * splits;

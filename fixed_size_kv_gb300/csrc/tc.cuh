@@ -58,8 +58,7 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 }
 // Bounded wait for the phase with the given parity; false if it gave up (after
 // WAIT_NS, or as soon as *abort_flag is set by another thread of the CTA).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                  bool cluster_scope = false);
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag);
 
 // ------------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* m) {
@@ -108,6 +107,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T, bf16 inputs, fp32 accumulation.  A is M = 128
+// rows in TMEM lanes 0..127 with K along the columns, two bf16 per 32-bit column
+// (the even-indexed element in the low half); B is given by its shared-memory descriptor.
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // Arrives on the mbarrier when every previously issued tcgen05.mma of this thread is done.
@@ -164,6 +174,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
         : "memory");
 }
+// 32 lanes x 16 consecutive 32-bit columns from registers into TMEM.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
@@ -198,21 +217,31 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, floa
 __device__ __forceinline__ void fence_acq_rel_cluster() {
     asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
 }
-// Arrive (release, cluster scope) on an mbarrier in another CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr)
-                 : "memory");
+// Arrive on an mbarrier in another CTA of the cluster, with the default (CTA-scope
+// release) semantics.  Used to hand a shared-memory buffer back to the peer that
+// fills it with st.async: the only ordering needed is that this CTA's reads of the
+// buffer come first, and the peer's bytes become visible here through the
+// complete_tx of the buffer's own mbarrier, not through this arrive.  (A
+// cluster-scope release would wait for every outstanding memory operation of the
+// thread, which costs about a microsecond per call.)
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
 }
-// Wait with acquire at cluster scope (the arrivals came from another CTA).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
+// Bulk copy (TMA engine) of `bytes` from this CTA's shared memory to shared memory of
+// a CTA of the cluster; completes `bytes` of transaction on that CTA's mbarrier.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+            dst_cluster),
+        "r"(src_cta), "r"(bytes), "r"(bar_cluster)
         : "memory");
-    return ok != 0;
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Waits until every bulk copy this thread committed has finished reading its source.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
@@ -241,28 +270,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16_bmn(int M, int N) {
     return idesc_bf16(M, N) | (1u << 16);
 }
 
-// Descriptor of an MN-major bf16 operand with 128-byte swizzling, as TMA writes a
-// [K rows][64 MN elements] tile: 8-row (8 K) groups 1024 B apart.  Used with an
-// N of 64 (one swizzle atom along MN), so the MN-direction offset is unused.
-__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr) {
+// Descriptor of an MN-major bf16 operand with 128-byte swizzling, as TMA writes
+// [K rows][64 MN elements] tiles: 8-row (8 K) groups 1024 B apart, and consecutive
+// 64-element MN atoms `mn_atom_bytes` apart (used when N > 64).
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr, uint32_t mn_atom_bytes = 16) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)1 << 16;                          // offset between MN atoms (unused at N = 64)
-    d |= (uint64_t)(1024 >> 4) << 32;                // offset between 8-row K groups
+    d |= (uint64_t)((mn_atom_bytes >> 4) & 0x3FFFu) << 16;   // offset between MN atoms
+    d |= (uint64_t)(1024 >> 4) << 32;                        // offset between 8-row K groups
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
 }
-
 }  // namespace snap
 
 namespace snap {
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                                  bool cluster_scope) {
-    if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > WAIT_NS) return false;

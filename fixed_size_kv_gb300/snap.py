@@ -62,6 +62,7 @@ SIGNATURES = {
     "snap_window_logits": (_I, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP]),
     "snap_decode_append": (_I, [_VP, _VP, _I, _VP, _VP, _VP]),
     "snap_decode_attn_ws_bytes": (_I, [_P(snap_config), _I, _P(_SZ)]),
+    "snap_decode_attn_plan": (_I, [_VP, _I, _P(_I), _P(_I), _P(_I)]),
     "snap_decode_attn": (_I, [_VP, _VP, _I, _VP, _VP, _VP, _SZ, _VP]),
     "snap_decode_step": (_I, [_VP, _VP, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "snap_check_device": (_I, [_VP, _VP]),
@@ -272,6 +273,13 @@ class SnapCache:
         assert out.dtype == torch.float32 and out.is_contiguous()
         return load().snap_decode_attn_noalloc(self.handle, _ptr(slots), slots.numel(), _ptr(q.contiguous()),
                                                _ptr(out), _stream(stream))
+
+    def decode_attn_plan(self, n: int):
+        """snap_decode_attn_plan: (splits, tiles_per_split, ctas_per_wave) for n sequences."""
+        sp, tp, wv = _I(), _I(), _I()
+        _check(load().snap_decode_attn_plan(self.handle, n, ctypes.byref(sp), ctypes.byref(tp), ctypes.byref(wv)),
+               "snap_decode_attn_plan")
+        return sp.value, tp.value, wv.value
 
     def check_device(self, stream=None) -> int:
         return load().snap_check_device(self.handle, _stream(stream))

@@ -193,6 +193,17 @@ snap_status snap_decode_append(snap_cache* cache, const int32_t* slots, int n, c
 snap_status snap_decode_attn_ws_bytes(const snap_config* cfg, int max_n, size_t* bytes);
 
 /*
+ * The launch plan snap_decode_attn() uses for a batch of n sequences on the current
+ * device: *splits key ranges per sequence (merged at the end when > 1), each walking
+ * *tiles_per_split key tiles (32 keys), and *ctas_per_wave CTAs of the attention
+ * kernel resident at once.  Host-side only (no kernel runs); for profiling and
+ * capacity planning.  SNAP_ERR_INVALID_ARG for a null pointer or n < 1,
+ * SNAP_ERR_CUDA when no device is current.
+ */
+snap_status snap_decode_attn_plan(const snap_cache* cache, int n, int* splits, int* tiles_per_split,
+                                  int* ctas_per_wave);
+
+/*
  * Split-KV decode attention over the fixed-size cache for a continuous batch whose
  * sequences sit at different ring offsets.  For each b < n and query head i, a plain
  * softmax over the VALID slots of sequence slots[b] (sinks < n_sink, middle < n_mid,

@@ -182,3 +182,19 @@ def test_decode_out_of_range_slot_reports_without_fault():
     assert b.cache.check_device() == snap.SNAP_ERR_DEVICE_CHECK
     assert float(out.float().abs().sum()) == 0.0
     assert b.cache.check_device() == snap.SNAP_OK  # cleared by the previous read
+
+
+@pytest.mark.parametrize("mla", [False, True])
+def test_decode_plan_covers_every_tile(mla):
+    """snap_decode_attn_plan: splits x tiles per split covers the cache, every split is
+    non-empty, and a wave holds at least one CTA."""
+    if mla:
+        wl = inputs.Workload("mla_mid", 1, 128, 1, 576, 512, 64, 960, 3072, 8, 7, 1, 0, 0, 0, 1 / math.sqrt(192))
+    else:
+        wl = inputs.Workload("cb", 0, 32, 8, 128, 128, 4, 2044, 2048, 16, 7, 5, 0, 0, 0, 1 / math.sqrt(128))
+    cache = snap.SnapCache(snap_cfg(wl), max_batch=8, max_prompt=64)
+    tiles = -(-cache.C // 32)
+    for n in (1, 3, 8):
+        splits, per, wave = cache.decode_attn_plan(n)
+        assert 1 <= splits <= 32 and wave >= 1
+        assert splits * per >= tiles and (splits - 1) * per < tiles
