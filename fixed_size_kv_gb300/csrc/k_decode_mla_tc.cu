@@ -9,25 +9,26 @@
 // A cluster of two CTAs handles one (sequence, split) and divides the 576 columns:
 //   rank 0 owns columns   0..255 (4 chunks of 64): its part of q.k and values 0..255
 //   rank 1 owns columns 256..575 (5 chunks):       its part of q.k and values 256..511
-// Per 32-key tile, each CTA computes its partial scores S_r = Q_r K_r^T into TMEM,
+// Per 64-key tile, each CTA computes its partial scores S_r = Q_r K_r^T into TMEM,
 // the two exchange their partials through distributed shared memory (both then hold
 // the same S = S_0 + S_1), run the same online softmax (same max, same rounded
 // weights), and each accumulates its half of O = P V in TMEM (256 fp32 columns).
 // No score is computed twice and each cache byte is read by one CTA only.
 //
-// The A operands of both products live in TMEM: this CTA's part of Q (loaded once)
-// and the bf16 weights P of each tile (written there by the softmax), so the
-// tensor core reads only the cache tile from shared memory.  TMEM columns:
-// scores 0..63 (two 32-key buffers), P 64..95 (two 32-key buffers), Q 96..255
-// (up to 5 chunks of 64 bf16), this CTA's half of O 256..511.
+// A tcgen05.mma with a small N costs about as much as one with N = 64, so the
+// instruction count per key sets the pace: scores use N = 64 keys per MMA and P V
+// uses N = 256 (all four value chunks of the CTA in one MMA).  Operand A comes from
+// TMEM where it fits: the four latent chunks of q (rank 1's rope chunk sits in
+// shared memory) and the bf16 weights P, written over the scores they came from.
+// TMEM columns: scores / weights 0..127 (one 64-column buffer per softmax group),
+// q 128..255, this CTA's half of O 256..511.
 //
 // Roles (320 threads per CTA): warp 0 issues TMA loads (and L2 prefetches ahead),
 // warp 1 owns TMEM and one thread issues tcgen05.mma from two queues (scores of the
 // next tile, P V of the oldest ready tile).  Warps 2..9 run the softmax as two
 // groups of four warps (one TMEM lane quarter each; thread = head) that take
 // alternate tiles, so two tiles are in the softmax at once: while one group waits
-// for the peer's partial scores, the other computes weights.  Each group has its
-// own score buffer, exchange buffers and weight buffer.
+// for the peer's partial scores, the other computes weights.
 //
 // Both groups accumulate into the one O in TMEM, so they share one running max.
 // It is handed from the group of tile i-1 to the group of tile i (per lane
@@ -45,38 +46,38 @@ namespace {
 constexpr float NEG_INF = -__builtin_huge_valf();
 constexpr int MV = 512;                     // value (latent) width
 constexpr int HEADS = 128;                  // M of every MMA
-constexpr int TK = 32;                      // keys per tile
-constexpr int CH_B = TK * 128;              // one 64-column chunk of a KV tile: 4 KB
+constexpr int TK = 64;                      // keys per tile
+constexpr int CH_B = TK * 128;              // one 64-column chunk of a KV tile: 8 KB
 constexpr int MAXCH = 5;                    // chunks owned by rank 1
-constexpr int KST = 6;                      // KV tile stages
+constexpr int KST = 3;                      // KV tile stages
 constexpr int NG = 2;                       // softmax groups (tile i goes to group i % 2)
 constexpr int THREADS = 64 + NG * 128;
 constexpr float RESCALE_GAP = 32.f;         // weights up to 2^32 stay exact in fp32 O and l
-constexpr int XROW_B = TK * 4;              // one head's partial scores: 128 B
-constexpr int XBUF_B = HEADS * XROW_B;      // one tile's partial scores: 16 KB
+constexpr int XROW_B = TK * 4;              // one head's partial scores: 256 B
+constexpr int XBUF_B = HEADS * XROW_B;      // one tile's partial scores: 32 KB
 
 constexpr int OFF_KV = 0;
-constexpr int OFF_X = OFF_KV + KST * MAXCH * CH_B;        // 120 KB
-constexpr int OFF_XS = OFF_X + NG * XBUF_B;               // + 32 KB (incoming partial scores, per group)
-constexpr int OFF_ML = OFF_XS + NG * XBUF_B;              // + 32 KB (outgoing partial scores, per group)
-constexpr int OFF_BAR = OFF_ML + 2048;                    // + running max [128] and group sums [2][128]
+constexpr int OFF_QR = OFF_KV + KST * MAXCH * CH_B;       // 120 KB
+constexpr int OFF_X = OFF_QR + HEADS * 128;               // + 16 KB (rank 1's rope chunk of q)
+constexpr int OFF_ML = OFF_X + NG * XBUF_B;               // + 64 KB (incoming partial scores, per group)
+constexpr int OFF_BAR = OFF_ML + 1536;                    // + running max [128] and group sums [2][128]
 constexpr int SMEM = OFF_BAR + 256 + 1024;                // barriers + alignment slack
 
 enum {
     B_Q_FULL = 0,
     B_KV_FULL = 1,               // + KST
     B_KV_EMPTY = 1 + KST,        // + KST
-    B_S_FULL = 1 + 2 * KST,      // + NG
-    B_S_EMPTY = 3 + 2 * KST,     // + NG
-    B_P_FULL = 5 + 2 * KST,      // + NG
-    B_P_EMPTY = 7 + 2 * KST,     // + NG
-    B_X_FULL = 9 + 2 * KST,      // + NG
-    B_X_EMPTY = 11 + 2 * KST,    // + NG
-    B_M_READY = 13 + 2 * KST,    // + 4 (one per lane quarter)
-    N_BARS = 17 + 2 * KST
+    B_S_FULL = 1 + 2 * KST,      // + NG: scores of the group's tile are in TMEM
+    B_SP_EMPTY = 3 + 2 * KST,    // + NG: P V of the group's previous tile done (buffer free)
+    B_P_FULL = 5 + 2 * KST,      // + NG: weights of the group's tile are in TMEM
+    B_X_FULL = 7 + 2 * KST,      // + NG
+    B_X_EMPTY = 9 + 2 * KST,     // + NG
+    B_M_READY = 11 + 2 * KST,    // + 4 (one per lane quarter)
+    N_BARS = 15 + 2 * KST
 };
 static_assert((N_BARS + 1) * 8 <= 256, "barrier area");
 static_assert(SMEM <= 232448, "shared memory");
+static_assert(TK == 64, "the mask below takes two 32-key ballots");
 
 constexpr int SOFTMAX_BAR_ID = 1;           // named barrier of the softmax warps (bar 0 = __syncthreads)
 
@@ -93,11 +94,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const uint32_t peer = rank ^ 1u;
     const int split = blockIdx.x >> 1, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nch = rank == 0 ? 4 : 5;          // chunks owned
+    const int nch = rank == 0 ? 4 : 5;          // chunks owned (the last of rank 1's is the rope)
     const int c0 = rank == 0 ? 0 : 4;           // first owned chunk
 
     const uint32_t s_base = smem_u32(smem);
-    const uint32_t s_kv = s_base + OFF_KV, s_x = s_base + OFF_X;
+    const uint32_t s_kv = s_base + OFF_KV, s_qr = s_base + OFF_QR, s_x = s_base + OFF_X;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     auto bar = [&](int i) { return smem_u32(bars + i); };
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + N_BARS);
@@ -109,18 +110,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const bool slot_ok = slot >= 0 && slot < c.max_batch;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(B_Q_FULL), NG * 4);      // the softmax warps, after storing Q into TMEM
+        mbar_init(bar(B_Q_FULL), NG * 4);      // the softmax warps, after storing q
         for (int i = 0; i < KST; ++i) {
             mbar_init(bar(B_KV_FULL + i), 1);
             mbar_init(bar(B_KV_EMPTY + i), 1);
         }
         for (int g = 0; g < NG; ++g) {
             mbar_init(bar(B_S_FULL + g), 1);
-            mbar_init(bar(B_S_EMPTY + g), 4);
-            mbar_init(bar(B_X_FULL + g), 1);    // this CTA's expect_tx + the peer's bulk-copy bytes
-            mbar_init(bar(B_X_EMPTY + g), 4);   // the peer's four warps of group g
+            mbar_init(bar(B_SP_EMPTY + g), 1);
             mbar_init(bar(B_P_FULL + g), 4);
-            mbar_init(bar(B_P_EMPTY + g), 1);
+            mbar_init(bar(B_X_FULL + g), 1);    // this CTA's expect_tx + the peer's st.async bytes
+            mbar_init(bar(B_X_EMPTY + g), 4);   // the peer's four warps of group g
         }
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_M_READY + q), 1);
         *abort_flag = 0;
@@ -134,8 +134,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     cluster_sync_all();                 // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    // TMEM: scores (one 32-column buffer per group), P (one 16-column buffer per group), Q, O
-    const uint32_t T_S = tmem, T_P = tmem + 64, T_Q = tmem + 96, T_O = tmem + 256;
+    // TMEM: scores, then weights (one 64-column buffer per group), q, O
+    const uint32_t T_S = tmem, T_Q = tmem + 128, T_O = tmem + 256;
 
     // status detail: 300 + rank, the wait that gave up, the tile index reached
     int cur_tile = -1;
@@ -164,7 +164,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && t_begin < t_end) {
             tma_prefetch(&tmKV);
-            constexpr int AHEAD = 8;    // tiles on their way to L2 ahead of the loads
+            constexpr int AHEAD = 4;    // tiles on their way to L2 ahead of the loads
             for (int t = t_begin; t < min(t_end, t_begin + AHEAD); ++t)
                 for (int j = 0; j < nch; ++j) tma_prefetch_3d(&tmKV, 64 * (c0 + j), t * TK, slot);
             int i = 0;
@@ -188,24 +188,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const uint32_t id_pv = idesc_bf16_bmn(HEADS, 256);   // all four value chunks per MMA
             bool ok = wait_bar(bar(B_Q_FULL), 0, abort_flag);
             if (!ok) fail(10);
-            // Two queues: the scores of the next tile (needs its KV and a free score
-            // buffer) and P V of the oldest tile with weights ready.  Issue whichever is
-            // ready, so P V never waits behind the next tile's data.
+            // Two queues: the scores of the next tile (needs its KV and its group's
+            // buffer back from P V two tiles ago) and P V of the oldest tile with
+            // weights ready.  Issue whichever is ready.
             int n_t = 0;
             for (int t = next_tile(t_begin); t < t_end; t = next_tile(t + 1)) ++n_t;
             int qk = 0, pv = 0;
             uint64_t t_idle = 0;
             while (ok && pv < n_t) {
                 bool progressed = false;
-                if (qk < n_t && mbar_test_wait(bar(B_S_EMPTY + (qk & 1)), ((qk >> 1) & 1) ^ 1) &&
+                if (qk < n_t && mbar_test_wait(bar(B_SP_EMPTY + (qk & 1)), ((qk >> 1) & 1) ^ 1) &&
                     mbar_test_wait(bar(B_KV_FULL + qk % KST), (qk / KST) & 1)) {
                     tc_fence_after();
                     const int st = qk % KST, sb = qk & 1;
-                    for (int j = 0; j < nch; ++j)
+                    const uint32_t d = T_S + sb * TK;
+                    for (int j = 0; j < 4; ++j)         // latent chunks: q from TMEM
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)     // 16 columns (8 TMEM columns of Q) per step
-                            tc_mma_ta(T_S + sb * TK, T_Q + j * 32 + k * 8,
-                                      desc_sw128(s_kv + (st * MAXCH + j) * CH_B + k * 32), id_qk, (j | k) ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k)     // 16 columns (8 TMEM columns of q) per step
+                            tc_mma_ta(d, T_Q + j * 32 + k * 8, desc_sw128(s_kv + (st * MAXCH + j) * CH_B + k * 32),
+                                      id_qk, (j | k) ? 1u : 0u);
+                    if (nch == 5)                       // rank 1's rope chunk: q from shared memory
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma(d, desc_sw128(s_qr + k * 32), desc_sw128(s_kv + (st * MAXCH + 4) * CH_B + k * 32),
+                                   id_qk, 1u);
                     tc_commit(bar(B_S_FULL + sb));
                     ++qk;
                     progressed = true;
@@ -213,13 +219,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 if (pv < qk && mbar_test_wait(bar(B_P_FULL + (pv & 1)), (pv >> 1) & 1)) {
                     tc_fence_after();
                     const int stp = pv % KST;
-                    const uint32_t pa = T_P + (pv & 1) * (TK / 2);  // this tile's weights
+                    const uint32_t pa = T_S + (pv & 1) * TK;  // the weights, written over the scores
                     // N = 256: this CTA's four 64-column value chunks (CH_B apart) in one MMA
 #pragma unroll
                     for (int k = 0; k < TK / 16; ++k)       // 16 keys (8 TMEM columns of P) per step
                         tc_mma_ta(T_O, pa + k * 8, desc_sw128_mn(s_kv + stp * MAXCH * CH_B + k * 2048, CH_B), id_pv,
                                   (pv > 0 || k > 0) ? 1u : 0u);
-                    tc_commit(bar(B_P_EMPTY + (pv & 1)));
+                    tc_commit(bar(B_SP_EMPTY + (pv & 1)));
                     tc_commit(bar(B_KV_EMPTY + stp));
                     ++pv;
                     progressed = true;
@@ -241,16 +247,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const int quarter = warp & 3;           // TMEM lane quarter this warp may access
         const int row = quarter * 32 + lane;    // query head
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t t_buf = T_S + lane_off + g * TK;    // this group's score / weight buffer
         const float sl2 = c.scale_log2;
-        const uint32_t s_xs_warp = s_base + OFF_XS + g * XBUF_B + quarter * 32 * XROW_B;
         const uint32_t m_ready = bar(B_M_READY + quarter);
         bool ok = true;
 
-        // This CTA's columns of q (64-column chunks c0 .. c0+nch-1) into TMEM, one
-        // head per lane; the two groups take alternate chunks.
+        // q: the latent chunks of this CTA into TMEM (one head per lane, the two groups
+        // take alternate chunks), rank 1's rope chunk into shared memory as a 128-byte
+        // swizzled K-major tile (group 1 writes it).
         {
             const bf16* qrow = a.q + ((size_t)b * c.Hq + row) * (size_t)c.dqk + 64 * c0;
-            for (int j = g; j < nch; j += NG) {
+            for (int j = g; j < 4; j += NG) {
                 const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * j);
                 float v[32];
 #pragma unroll
@@ -263,6 +270,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 }
                 tmem_st32(T_Q + lane_off + 32 * j, v);
             }
+            if (nch == 5 && g == 1) {
+                const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * 4);
+                const uint32_t dst = s_qr + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint4 u = src[e];
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + ((e ^ (row & 7)) << 4)),
+                                 "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w)
+                                 : "memory");
+                }
+                fence_proxy_async();
+            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -270,35 +289,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
 
         // Sends tile j's partial scores (in registers) into the peer's exchange buffer
-        // of this group: the warp stages its 32 rows in shared memory and one lane
-        // hands the 4 KB to the TMA engine as one bulk copy into the peer.  The 16-byte
-        // chunks of a 128-byte row are XOR-swizzled by row so that a warp reading or
-        // writing chunk k of 32 rows hits distinct banks.
+        // of this group with st.async; the 16-byte chunks of a 256-byte row are
+        // XOR-swizzled by row so that a warp reading chunk k of 32 rows spreads over
+        // the banks.
         auto send = [&](int j, const float (&s)[TK]) -> bool {
-            // the bulk copy of this group's previous tile has finished reading the staging rows
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
-            const uint32_t srow = s_xs_warp + lane * XROW_B;
-#pragma unroll
-            for (int k = 0; k < TK / 4; ++k)
-                asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};\n" ::"r"(srow + 16 * (k ^ (row & 7))),
-                             "f"(s[4 * k]), "f"(s[4 * k + 1]), "f"(s[4 * k + 2]), "f"(s[4 * k + 3])
-                             : "memory");
-            fence_proxy_async();
+            // the peer has consumed what this group sent for its previous tile
+            if (!__all_sync(0xffffffffu, wait_bar(bar(B_X_EMPTY + g), ((j >> 1) & 1) ^ 1, abort_flag))) return false;
             // the peer's scores of tile j will land in this group's buffer: announce the bytes
             if (quarter == 0 && lane == 0) mbar_expect_tx(bar(B_X_FULL + g), XBUF_B);
-            __syncwarp();
-            bool ok_send = true;
-            if (lane == 0) {
-                // the peer has consumed what this group sent for its previous tile
-                ok_send = wait_bar(bar(B_X_EMPTY + g), ((j >> 1) & 1) ^ 1, abort_flag);
-                if (ok_send) {
-                    bulk_copy_to_cluster(mapa(s_x + g * XBUF_B + quarter * 32 * XROW_B, peer), s_xs_warp,
-                                         32 * XROW_B, mapa(bar(B_X_FULL + g), peer));
-                    bulk_commit();
-                }
-            }
-            return __shfl_sync(0xffffffffu, ok_send, 0);
+            const uint32_t dst = mapa(s_x + g * XBUF_B + row * XROW_B, peer);
+            const uint32_t xfull_peer = mapa(bar(B_X_FULL + g), peer);
+#pragma unroll
+            for (int k = 0; k < TK / 4; ++k)
+                st_async_v4(dst + 16 * (k ^ (row & 7)), s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3], xfull_peer);
+            return true;
         };
 
         float m_used = NEG_INF;     // the running max this group's sum l_g is relative to
@@ -316,11 +320,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 continue;
             }
             tc_fence_after();
-            tmem_ld32(T_S + lane_off + g * TK, s);
-            tmem_ld_wait(s);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_S_EMPTY + g));
+            {
+                float lo[32], hi[32];
+                tmem_ld32(t_buf, lo);
+                tmem_ld32(t_buf + 32, hi);
+                tmem_ld_wait(lo);
+                tmem_ld_wait(hi);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    s[k] = lo[k];
+                    s[32 + k] = hi[k];
+                }
+            }
             // 2. to the peer
             if (!send(i, s)) {
                 fail(6);
@@ -345,13 +356,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(mapa(bar(B_X_EMPTY + g), peer));
-            // 4. mask (one ballot for the tile's 32 slots), scale, tile max
-            const uint32_t vmask = __ballot_sync(0xffffffffu, t * TK + lane < c.C && sv.valid(t * TK + lane));
+            // 4. mask (two ballots for the tile's 64 slots), scale, tile max
+            const uint32_t v0 = __ballot_sync(0xffffffffu, t * TK + lane < c.C && sv.valid(t * TK + lane));
+            const uint32_t v1 =
+                __ballot_sync(0xffffffffu, t * TK + 32 + lane < c.C && sv.valid(t * TK + 32 + lane));
             float mt = NEG_INF;
 #pragma unroll
-            for (int k = 0; k < TK; ++k) {
-                s[k] = ((vmask >> k) & 1u) ? s[k] * sl2 : NEG_INF;
-                mt = fmaxf(mt, s[k]);
+            for (int k = 0; k < 32; ++k) {
+                s[k] = ((v0 >> k) & 1u) ? s[k] * sl2 : NEG_INF;
+                s[32 + k] = ((v1 >> k) & 1u) ? s[32 + k] * sl2 : NEG_INF;
+                mt = fmaxf(mt, fmaxf(s[k], s[32 + k]));
             }
             // 5. the running max as left by tile i-1 (the other group)
             float m_prev = NEG_INF;
@@ -371,9 +385,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             const float m_new = move ? fmaxf(mt, m_prev) : m_prev;
             const bool rescale_lane = move && m_prev != NEG_INF;
             if (__any_sync(0xffffffffu, rescale_lane)) {
-                // a lane with a finite running max saw weights in an earlier tile: i >= 1
+                // a lane with a finite running max saw weights in an earlier tile: i >= 1.
+                // (The scores of tile i-1 waited for P V of tile i-3, so the other
+                // group's buffer barrier is at most one phase behind this wait.)
                 if (!__all_sync(0xffffffffu,
-                                wait_bar(bar(B_P_EMPTY + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag))) {
+                                wait_bar(bar(B_SP_EMPTY + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag))) {
                     fail(5);
                     ok = false;
                     continue;
@@ -392,14 +408,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 tmem_st_wait();
                 tc_fence_before();
             }
-            // 6. this group's half of P is free once P V of its previous tile is done
-            if (!__all_sync(0xffffffffu, wait_bar(bar(B_P_EMPTY + g), (k_g & 1) ^ 1, abort_flag))) {
-                fail(7);
-                ok = false;
-                continue;
-            }
-            // 7. hand the running max to tile i+1 (after the wait above, so that the
-            //    other group's waits on this group's P barrier see its current phase)
+            // 6. hand the running max to tile i+1
             m_sh[row] = m_new;
             __syncwarp();
             if (lane == 0) mbar_arrive(m_ready);
@@ -407,17 +416,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 l_g = m_used == NEG_INF ? l_g : l_g * ex2(m_used - m_new);
                 m_used = m_new;
             }
-            // 8. weights (bf16, two keys per TMEM column) into this group's P buffer
-            uint32_t w[TK / 2];
+            // 7. weights (bf16, two keys per TMEM column) over this group's scores (read
+            //    above, so the buffer is free until P V of this tile releases it)
+            float w[32];
             float psum = 0.f;
 #pragma unroll
             for (int e = 0; e < TK / 2; ++e) {
                 const float p0 = m_new == NEG_INF ? 0.f : bf16_round(ex2(s[2 * e] - m_new));
                 const float p1 = m_new == NEG_INF ? 0.f : bf16_round(ex2(s[2 * e + 1] - m_new));
                 psum += p0 + p1;
-                w[e] = pack_bf16(p0, p1);
+                w[e] = __uint_as_float(pack_bf16(p0, p1));
             }
-            tmem_st16(T_P + lane_off + g * (TK / 2), w);
+            tmem_st32(t_buf, w);
             tmem_st_wait();
             tc_fence_before();
             l_g += psum;
@@ -426,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         const int n_t = i;
 
-        // 9. the final running max (from the group of the last tile) and P V of the
+        // 8. the final running max (from the group of the last tile) and P V of the
         //    last tile done (its commit covers every earlier MMA too)
         float m_fin = NEG_INF;
         if (ok && n_t > 0) {
@@ -435,7 +445,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 fail(8);
                 ok = false;
             }
-            if (ok && !__all_sync(0xffffffffu, wait_bar(bar(B_P_EMPTY + ((n_t - 1) & 1)), ((n_t - 1) >> 1) & 1,
+            if (ok && !__all_sync(0xffffffffu, wait_bar(bar(B_SP_EMPTY + ((n_t - 1) & 1)), ((n_t - 1) >> 1) & 1,
                                                         abort_flag))) {
                 fail(8);
                 ok = false;
@@ -448,7 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         asm volatile("bar.sync %0, %1;\n" ::"n"(SOFTMAX_BAR_ID), "n"(NG * 128) : "memory");
         const float l_run = l_sh[row] + l_sh[HEADS + row];
 
-        // 10. this CTA's half of the output; group g writes TMEM columns 128 g .. 128 g + 127
+        // 9. this CTA's half of the output; group g writes TMEM columns 128 g .. 128 g + 127
         if (ok && row < c.Hq) {
             const int head = row;
             const int d0 = rank == 0 ? 0 : 256;
@@ -481,7 +491,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 a.part_ml[pi * 2 + 1] = l_run;
             }
         }
-        if (lane == 0) bulk_wait_read_all();    // the staging rows stay until their last copy has read them
     }
 
     __syncthreads();

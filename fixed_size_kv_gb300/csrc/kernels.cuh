@@ -27,11 +27,11 @@ struct DecodeArgs {
 };
 
 constexpr int GQA_KEYS = 32;     // keys per warp step of the GQA decode kernel
-constexpr int MLA_KEYS = 32;     // keys per tile of the MLA decode kernel
+constexpr int MLA_KEYS = 64;     // keys per tile of the MLA decode kernel
 constexpr int MLA_HEADS = 128;   // query heads of the MLA layout (the M of its MMAs)
 
 cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
-// tkv: cache [max_batch][C][576], box {64, 32, 1} (queries are read from a.q directly)
+// tkv: cache [max_batch][C][576], box {64, 64, 1} (queries are read from a.q directly)
 cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cudaStream_t st);
 // CTAs of the MLA decode kernel that can be resident at once on the current device
 // (two per co-resident cluster; 0 if the occupancy query fails).

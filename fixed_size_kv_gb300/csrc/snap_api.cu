@@ -203,7 +203,7 @@ cudaError_t run_rowstat(int mode, const snap_config& c, ScoreParams sp, const vo
     return launch_score_tc(mode, tx, ty, sp, c.d_qk, true, true, num_sms(), st);
 }
 
-// MLA decode tensor map of the cache rows [max_batch][C][576] (box 64 x 32).
+// MLA decode tensor map of the cache rows [max_batch][C][576] (box 64 x 64).
 bool mla_cache_map(CUtensorMap* tkv, const snap_cache* cache);
 
 // Split count and launches of one decode-attention call (shared by the entry points).
@@ -262,6 +262,27 @@ int decode_splits(int base, int tiles, int wave) {
     return best;
 }
 
+// MLA decode: each CTA also pays a fixed cost (TMEM and cluster setup, the q load,
+// writing its partial output) worth about this many 64-key tiles, so its split
+// count minimises waves x (tiles per split + that cost) instead.
+constexpr int MLA_FIXED_TILES = 8;
+
+int decode_splits_fixed_cost(int base, int tiles, int wave, int fixed_tiles) {
+    int best = 1;
+    long long best_cost = -1;
+    for (int s = 1; s <= MAX_DECODE_SPLITS; ++s) {
+        const int per = (tiles + s - 1) / s;
+        if (s > 1 && per < 4) break;
+        const long long waves = ((long long)base * s + wave - 1) / wave;
+        const long long cost = waves * (per + fixed_tiles);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
 // CTAs of one decode-attention kernel resident at once: one per SM for GQA; for MLA
 // two per co-resident cluster (the GPCs may leave SMs that cannot host a pair).
 int decode_wave_ctas(const snap_cache* cache) {
@@ -271,7 +292,7 @@ int decode_wave_ctas(const snap_cache* cache) {
 }
 
 // Splits of one decode-attention call: enough CTAs for whole waves (GQA: 4 warps walk
-// a split, one 32-key tile each per step; MLA: two CTAs per split, 32-key tiles).
+// a split, one 32-key tile each per step; MLA: two CTAs per split, 64-key tiles).
 int decode_split_count(const snap_cache* cache, int n) {
     const snap_config& c = cache->cfg;
     if (c.layout == SNAP_LAYOUT_GQA) {
@@ -279,7 +300,7 @@ int decode_split_count(const snap_cache* cache, int n) {
         return decode_splits(n * c.n_kv_heads, tiles / 4, decode_wave_ctas(cache));
     }
     const int tiles = (int)((cache->C + MLA_KEYS - 1) / MLA_KEYS);
-    return decode_splits(2 * n, tiles, decode_wave_ctas(cache));
+    return decode_splits_fixed_cost(2 * n, tiles, decode_wave_ctas(cache), MLA_FIXED_TILES);
 }
 
 // Splits and key tiles per split of one decode-attention call: the split count is

@@ -193,7 +193,7 @@ def test_decode_plan_covers_every_tile(mla):
     else:
         wl = inputs.Workload("cb", 0, 32, 8, 128, 128, 4, 2044, 2048, 16, 7, 5, 0, 0, 0, 1 / math.sqrt(128))
     cache = snap.SnapCache(snap_cfg(wl), max_batch=8, max_prompt=64)
-    tiles = -(-cache.C // 32)
+    tiles = -(-cache.C // (64 if mla else 32))    # key tile of the MLA / GQA kernel
     for n in (1, 3, 8):
         splits, per, wave = cache.decode_attn_plan(n)
         assert 1 <= splits <= 32 and wave >= 1

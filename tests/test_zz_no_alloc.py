@@ -61,15 +61,27 @@ def test_noalloc_matches_workspace_entry_point_twice(layout):
         assert d.max().item() <= MAX_ABS and d.mean().item() <= MEAN_ABS, (step, d.max().item())
 
 
+def _scratch_need(n, heads, splits, d_v):
+    """Bytes of split partials one call needs: O rounded up to 256 B, then (max, sum)."""
+    parts = n * heads * splits
+    return -(-parts * 4 * d_v // 256) * 256 + parts * 4 * 2
+
+
 def test_noalloc_refuses_batches_beyond_its_scratch():
-    """128-head MLA at a 32768-slot cache needs more than the fixed scratch for 8
-    sequences: refused before any launch, nothing written."""
+    """128-head MLA at a 32768-slot cache: the first batch size whose split partials
+    (per the library's own launch plan) exceed the fixed scratch is refused before
+    any launch, and nothing is written."""
     wl = inputs.WORKLOADS["mla_128k_b8"]
     snap.load(build_if_missing=True)
-    cache = snap.SnapCache(_cfg(wl), max_batch=8, max_prompt=1)
-    slots = torch.arange(8, dtype=torch.int32, device="cuda")
-    q = torch.zeros((8, wl.n_q_heads, wl.d_qk), dtype=torch.bfloat16, device="cuda")
-    out = torch.full((8, wl.n_q_heads, wl.d_v), 7.0, dtype=torch.float32, device="cuda")
+    cache = snap.SnapCache(_cfg(wl), max_batch=64, max_prompt=1)
+    limit = 32 << 20    # SNAP_NOALLOC_SCRATCH_BYTES in include/snap.h
+    n = next((n for n in range(1, 65)
+              if _scratch_need(n, wl.n_q_heads, cache.decode_attn_plan(n)[0], wl.d_v) > limit
+              and cache.decode_attn_plan(n)[0] > 1), None)
+    assert n is not None, "no batch of up to 64 sequences overflows the scratch"
+    slots = torch.arange(n, dtype=torch.int32, device="cuda")
+    q = torch.zeros((n, wl.n_q_heads, wl.d_qk), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((n, wl.n_q_heads, wl.d_v), 7.0, dtype=torch.float32, device="cuda")
     assert cache.decode_attn_noalloc(slots, q, out) == snap.SNAP_ERR_SHAPE
     torch.cuda.synchronize()
     assert bool((out == 7.0).all())
