@@ -47,11 +47,19 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling)")
-    p.add_argument("--graph", action="store_true",
-                   help="replay the decode loop as one captured CUDA graph (small workloads)")
+    p.add_argument("--eager", action="store_true",
+                   help="launch the decode steps one by one instead of replaying them as one captured "
+                        "CUDA graph (the default: the decode loop has static shapes and no host sync)")
+    p.add_argument("--graph", action="store_true", help=argparse.SUPPRESS)  # the default; kept for old commands
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-full-kv", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--capacity", type=float, default=0.0, metavar="GIB",
+                   help="extra mode: the largest batch whose cache fits GIB of HBM, fixed-size cache vs full "
+                        "KV, with decode tok/s measured at that batch (one JSON line per cache kind)")
+    p.add_argument("--sweep", action="store_true",
+                   help="extra mode: decode tok/s over context length (fixed C = S/4 vs full KV) and over "
+                        "the cache composition (L_sink, K, L_recent) at 128k (one JSON line per case)")
     return p.parse_args()
 
 
@@ -220,7 +228,7 @@ def run_ours(args):
         one_step(cache, pre)
     barrier()
     graph = None
-    if args.graph:
+    if not args.eager:
         # the decode loop has static shapes and no host synchronisation: capture it once
         graph = torch.cuda.CUDAGraph()
         for b in range(B):
@@ -306,6 +314,21 @@ def run_ours(args):
         full_wl = wl.replace(L_sink=0, K=0, L_recent=max(lengths) + D)
         fcfg = snap.make_config(**full_wl.config_kwargs())
         fcache = snap.SnapCache(fcfg, max_batch=B, max_prompt=1, max_n=B, device=dev, stream=stream)
+
+        def f_decode():
+            for t in range(D):
+                fcache.decode_step(slots, q_all[t], k_all[t], v_all[t] if v_all is not None else None,
+                                   out=out[t], stream=stream)
+
+        fgraph = None
+        if not args.eager:  # the same launch mode as the fixed cache's decode loop
+            for b in range(B):
+                fcache.compress(b, pre[b].K, pre[b].V, pre[b].Q, stream=stream)
+            stream.synchronize()
+            fgraph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(fgraph, stream=stream):
+                f_decode()
+            stream.synchronize()
         runs = []
         for rep in range(2):
             for b in range(B):
@@ -323,14 +346,24 @@ def run_ours(args):
                 eb.append(bb)
             e1.record(stream)
             stream.synchronize()
-            runs.append((e0.elapsed_time(e1), sum(x.elapsed_time(y) for x, y in zip(ea, eb)) / D))
+            loop_ms = e0.elapsed_time(e1)
+            if fgraph is not None:  # the loop time from a replay (the attention time above stays per launch)
+                for b in range(B):
+                    fcache.compress(b, pre[b].K, pre[b].V, pre[b].Q, stream=stream)
+                e0.record(stream)
+                with torch.cuda.stream(stream):
+                    fgraph.replay()
+                e1.record(stream)
+                stream.synchronize()
+                loop_ms = e0.elapsed_time(e1)
+            runs.append((loop_ms, sum(x.elapsed_time(y) for x, y in zip(ea, eb)) / D))
         f_ms, f_attn = min(runs)
         fmetas = [(S, S + D // 2, 0, 0, 0) for S in lengths]
         f_bytes = algorithmic_decode_bytes(full_wl, fmetas)
         full = {"decode_tok_s": B * D * world / (f_ms / 1e3), "decode_ms_per_token_step": f_ms / D,
                 "attn_ms": f_attn, "attn_hbm_gbs": f_bytes / (f_attn / 1e3) / 1e9,
                 "cache_bytes": snap.cache_bytes(fcfg, B)}
-        del fcache
+        del fcache, fgraph
         torch.cuda.empty_cache()
 
     # ---------------------------------------------------------------- end to end
@@ -401,16 +434,22 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# source file of each decode-attention kernel whose DRAM traffic is on record
+KERNEL_SOURCES = {"gqa_decode_kernel": "k_decode.cu", "mla_decode_tc_kernel": "k_decode_mla_tc.cu"}
+
+
 def traffic_record(workload):
     """DRAM bytes per decode-attention launch from the committed ncu summary, if it was
     taken on the current kernel source (else None)."""
     path = os.path.join(ROOT, "profiles", "decode_attn_traffic.txt")
-    src = os.path.join(ROOT, "fixed_size_kv_gb300", "csrc", "k_decode.cu")
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         for line in open(path):
             parts = dict(kv.split("=", 1) for kv in line.split() if "=" in kv)
-            if parts.get("workload") == workload and parts.get("src") == digest:
+            if parts.get("workload") != workload or parts.get("kernel") not in KERNEL_SOURCES:
+                continue
+            src = os.path.join(ROOT, "fixed_size_kv_gb300", "csrc", KERNEL_SOURCES[parts["kernel"]])
+            digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            if parts.get("src") == digest:
                 return float(parts["bytes_per_launch"])
     except (OSError, ValueError, KeyError):
         pass
@@ -418,9 +457,12 @@ def traffic_record(workload):
 
 
 def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world, reduce_max):
-    """The same step through the public API with pinned HOST inputs: every step copies
-    the prompts and each decode step's q/k/v to the device and reads every decode
-    output back."""
+    """The same job through the public API with pinned HOST inputs: every step copies
+    its prompts and every decode step's q/k/v to the device and reads every decode output
+    back, all inside the timed region.  The copies run on a second stream into two sets
+    of device buffers: step i+1's inputs upload while step i computes (the first step's
+    upload is not hidden), and within a step each compression waits for its own prompt
+    only.  The outputs of a step's decode steps come back in one copy at its end."""
     import torch
     from fixed_size_kv_gb300 import snap
     B, D = wl.batch, wl.decode_steps
@@ -430,46 +472,75 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
     hq, hk = q_all.to("cpu").pin_memory(), k_all.to("cpu").pin_memory()
     hv = v_all.to("cpu").pin_memory() if v_all is not None else None
     hout = torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.float32).pin_memory()
-    dK = [torch.empty_like(p.K) for p in pre]
-    dV = [torch.empty_like(p.V) if p.V is not None else None for p in pre]
-    dQ = [torch.empty_like(p.Q) for p in pre]
-    dq, dk = torch.empty_like(q_all[0]), torch.empty_like(k_all[0])
-    dv = torch.empty_like(v_all[0]) if v_all is not None else None
-    dout = torch.empty((B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev)
+
+    def buffers():
+        return {"K": [torch.empty_like(p.K) for p in pre],
+                "V": [torch.empty_like(p.V) if p.V is not None else None for p in pre],
+                "Q": [torch.empty_like(p.Q) for p in pre],
+                "q": torch.empty_like(q_all), "k": torch.empty_like(k_all),
+                "v": torch.empty_like(v_all) if v_all is not None else None,
+                "up": [torch.cuda.Event() for _ in range(B)], "up_dec": torch.cuda.Event(),
+                "done": torch.cuda.Event(), "used": False}
+
+    sets = [buffers(), buffers()]
+    dout = torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev)
     cache = snap.SnapCache(cfg, max_batch=B, max_prompt=max(lengths), max_n=B, device=dev, stream=stream)
     slots = torch.arange(B, dtype=torch.int32, device=dev)
     h2d = sum(x.numel() * 2 for x in hK + hQ) + sum(x.numel() * 2 for x in hV if x is not None)
-    h2d += D * (dq.numel() + dk.numel() + (dv.numel() if dv is not None else 0)) * 2
-    d2h = D * dout.numel() * 4
+    h2d += (q_all.numel() + k_all.numel() + (v_all.numel() if v_all is not None else 0)) * 2
+    d2h = dout.numel() * 4
+    copy = torch.cuda.Stream(device=dev)
 
-    def step():
-        with torch.cuda.stream(stream):
+    def upload(st):
+        if st["used"]:
+            copy.wait_event(st["done"])     # the step that last used this set has finished
+        st["used"] = True
+        with torch.cuda.stream(copy):
             for b in range(B):
-                dK[b].copy_(hK[b], non_blocking=True)
-                if dV[b] is not None:
-                    dV[b].copy_(hV[b], non_blocking=True)
-                dQ[b].copy_(hQ[b], non_blocking=True)
-                cache.compress(b, dK[b], dV[b], dQ[b], stream=stream)
-            for t in range(D):
-                dq.copy_(hq[t], non_blocking=True)
-                dk.copy_(hk[t], non_blocking=True)
-                if dv is not None:
-                    dv.copy_(hv[t], non_blocking=True)
-                cache.decode_step(slots, dq, dk, dv, out=dout, stream=stream)
-                hout[t].copy_(dout, non_blocking=True)
-    steps = max(1, min(args.steps, 3))
-    step()
+                st["K"][b].copy_(hK[b], non_blocking=True)
+                if st["V"][b] is not None:
+                    st["V"][b].copy_(hV[b], non_blocking=True)
+                st["Q"][b].copy_(hQ[b], non_blocking=True)
+                st["up"][b].record(copy)
+            st["q"].copy_(hq, non_blocking=True)
+            st["k"].copy_(hk, non_blocking=True)
+            if st["v"] is not None:
+                st["v"].copy_(hv, non_blocking=True)
+            st["up_dec"].record(copy)
+
+    def compute(st):
+        for b in range(B):
+            stream.wait_event(st["up"][b])
+            cache.compress(b, st["K"][b], st["V"][b], st["Q"][b], stream=stream)
+        stream.wait_event(st["up_dec"])
+        for t in range(D):
+            cache.decode_step(slots, st["q"][t], st["k"][t], st["v"][t] if st["v"] is not None else None,
+                              out=dout[t], stream=stream)
+        with torch.cuda.stream(stream):
+            hout.copy_(dout, non_blocking=True)
+        st["done"].record(stream)
+
+    # untimed warm-up of both buffer sets
+    for w in range(2):
+        upload(sets[w])
+        compute(sets[w])
     stream.synchronize()
+    copy.synchronize()
+    steps = max(1, args.steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(steps):
-        step()
+    copy.wait_stream(stream)                # the timed region starts before the first upload
+    upload(sets[0])
+    for i in range(steps):
+        if i + 1 < steps:
+            upload(sets[(i + 1) % 2])
+        compute(sets[i % 2])
     e1.record(stream)
     stream.synchronize()
     ms = reduce_max(e0.elapsed_time(e1))
     del cache
     return {"value": B * D * steps * world / (ms / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps}
+            "d2h_bytes_per_step": d2h, "steps": steps, "overlap": "double-buffered inputs"}
 
 
 # ----------------------------------------------------------------------------- oracle
@@ -662,10 +733,134 @@ def run_mixed(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- extra modes
+def _decode_rate(cache, wl, B, S_list, seed, dev, stream, steps=32, warm=4):
+    """Decode tok/s of B sequences already compressed in `cache`: `steps` decode steps
+    replayed as one CUDA graph after `warm` eager ones (inputs resident on the device)."""
+    import torch
+    from fixed_size_kv_gb300 import inputs
+    slots = torch.arange(B, dtype=torch.int32, device=dev)
+    toks = [inputs.gen_decode(wl, B, step=t, seed=seed, device=dev) for t in range(steps)]
+    out = torch.empty((B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev)
+    for t in range(warm):
+        cache.decode_step(slots, toks[t].q, toks[t].k, toks[t].v, out=out, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for t in range(steps):
+            cache.decode_step(slots, toks[t].q, toks[t].k, toks[t].v, out=out, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    e1.record(stream)
+    stream.synchronize()
+    return B * steps / (e0.elapsed_time(e1) / 1e3)
+
+
+def _fill(cache, pool, B, stream):
+    for b in range(B):
+        p = pool[b % len(pool)]
+        cache.compress(b, p.K, p.V, p.Q, stream=stream)
+    stream.synchronize()
+
+
+def run_capacity(args):
+    """SURVEY f4 (pages: "Max Batch Size Unlocked"): at a fixed HBM budget for the
+    cache, the largest batch of the workload's prompt length for the fixed-size cache
+    and for full KV, and the decode tok/s measured at that batch.  Sequences are filled
+    from a pool of 4 seeded prompts (the decode cost depends on the cache, not on which
+    prompt filled it)."""
+    import torch
+    from fixed_size_kv_gb300 import inputs, snap
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    snap.load(build_if_missing=True)
+    stream = torch.cuda.Stream(device=dev)
+    wl = inputs.WORKLOADS[args.workload]
+    S = wl.prompt_max
+    budget = int(args.capacity * (1 << 30))
+    with torch.cuda.stream(stream):
+        pool = [inputs.gen_prefill(wl, S, seed=args.seed, seq=i, device=dev) for i in range(4)]
+    stream.synchronize()
+    rates = {}
+    for kind in ("fixed", "full_kv"):
+        kwl = wl if kind == "fixed" else wl.replace(L_sink=0, K=0, L_recent=S + 64)
+        cfg = snap.make_config(**kwl.config_kwargs())
+        per_seq = snap.cache_bytes(cfg, 2) - snap.cache_bytes(cfg, 1)
+        B = budget // per_seq
+        if B < 1:
+            print(json.dumps({"mode": "capacity", "cache": kind, "max_batch": 0, "budget_gib": args.capacity}))
+            continue
+        cache = snap.SnapCache(cfg, max_batch=B, max_prompt=S, max_n=B, device=dev, stream=stream)
+        _fill(cache, pool, B, stream)
+        rate = _decode_rate(cache, kwl, B, [S] * B, args.seed, dev, stream)
+        rates[kind] = rate
+        print(json.dumps({"mode": "capacity", "workload": wl.name, "cache": kind, "budget_gib": args.capacity,
+                          "prompt_len": S, "cache_slots": kwl.C, "bytes_per_seq": per_seq, "max_batch": int(B),
+                          "decode_tok_s": rate, "data": "synthetic"}), flush=True)
+        del cache
+        torch.cuda.empty_cache()
+    if len(rates) == 2:
+        print(json.dumps({"mode": "capacity", "workload": wl.name, "budget_gib": args.capacity,
+                          "throughput_ratio_fixed_over_full": rates["fixed"] / rates["full_kv"]}), flush=True)
+
+
+def run_sweep(args):
+    """decode tok/s of a batch of 16 GQA (Llama-3.1-8B shape) sequences
+    (a) over context length with the cache at a quarter of the prompt (4 sinks, half
+    recent) against full KV (the pages' "Throughput by Context Length"), and (b) over the
+    cache composition (L_sink, K, L_recent) at 128k, K = 0 being StreamingLLM alone (the
+    axes of the pages' hyperparameter ablation)."""
+    import torch
+    from fixed_size_kv_gb300 import inputs, snap
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    snap.load(build_if_missing=True)
+    stream = torch.cuda.Stream(device=dev)
+    base = inputs.WORKLOADS["gqa_128k_b16"]
+    B = base.batch
+
+    def measure(wl, S, pool, tag):
+        cfg = snap.make_config(**wl.config_kwargs())
+        cache = snap.SnapCache(cfg, max_batch=B, max_prompt=S, max_n=B, device=dev, stream=stream)
+        _fill(cache, pool, B, stream)
+        rate = _decode_rate(cache, wl, B, [S] * B, args.seed, dev, stream)
+        del cache
+        torch.cuda.empty_cache()
+        return rate
+
+    for S in (32768, 65536, 131072):
+        with torch.cuda.stream(stream):
+            pool = [inputs.gen_prefill(base, S, seed=args.seed, seq=i, device=dev) for i in range(B)]
+        stream.synchronize()
+        C = S // 4
+        fixed = base.replace(L_sink=4, K=C // 2 - 4, L_recent=C // 2)
+        r_fixed = measure(fixed, S, pool, "fixed")
+        r_full = measure(base.replace(L_sink=0, K=0, L_recent=S + 64), S, pool, "full")
+        print(json.dumps({"mode": "sweep", "axis": "context", "prompt_len": S, "batch": B,
+                          "cache": f"4+{C // 2 - 4}+{C // 2}={C}", "decode_tok_s": r_fixed,
+                          "full_kv_decode_tok_s": r_full, "speedup": r_fixed / r_full}), flush=True)
+    S = 131072
+    for (ls, k, lr) in ((4, 16380, 16384), (0, 16384, 16384), (64, 16320, 16384), (4, 8188, 24576),
+                        (4, 24572, 8192), (4, 0, 32764)):
+        wl = base.replace(L_sink=ls, K=k, L_recent=lr)
+        r = measure(wl, S, pool, "mix")
+        print(json.dumps({"mode": "sweep", "axis": "composition", "prompt_len": S, "batch": B,
+                          "L_sink": ls, "K": k, "L_recent": lr, "decode_tok_s": r,
+                          "note": "StreamingLLM only" if k == 0 else ""}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.capacity > 0:
+        run_capacity(args)
+        return
+    if args.sweep:
+        run_sweep(args)
         return
     from fixed_size_kv_gb300 import inputs
     if inputs.WORKLOADS[args.workload].arrival_every > 0:
