@@ -656,9 +656,15 @@ def run_mixed(args):
     cache = snap.SnapCache(cfg, max_batch=B, max_prompt=wl.prompt_max, max_n=B, device=dev, stream=sa)
     out = torch.empty((B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev)
 
+    # valid cache slots of each slot's request: min(S, C) (every prompt covers sinks + ring)
+    valid = [0] * B
+    row_bytes = wl.n_kv_heads * (wl.d_qk + (wl.d_v if wl.layout == 0 else 0)) * 2
+    tok_bytes = wl.n_q_heads * (wl.d_qk * 2 + wl.d_v * 4)
+
     def compress(slot, req, stream):
         p = pool[req % NP]
         S = lengths[req]
+        valid[slot] = min(S, wl.C)
         cache.compress(slot, p.K[:S], p.V[:S] if p.V is not None else None, p.Q, stream=stream)
 
     def run(steps, timed):
@@ -673,6 +679,7 @@ def run_mixed(args):
         ev_b = None
         tokens = 0
         n_compress = 0
+        dec_bytes = 0
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(sa)
         active = [s for s in range(B) if remaining[s] > 0]
@@ -702,6 +709,7 @@ def run_mixed(args):
                 cache.decode_step(slots_t, tk.q[:n], tk.k[:n], tk.v[:n] if tk.v is not None else None,
                                   out=out[:n], stream=sa)
                 tokens += n
+                dec_bytes += sum(valid[s] for s in active) * row_bytes + n * tok_bytes
                 done = False
                 for s in active:
                     remaining[s] -= 1
@@ -712,12 +720,14 @@ def run_mixed(args):
                         slots_t = torch.tensor(active, dtype=torch.int32).to(dev, non_blocking=True)
         e1.record(sa)
         torch.cuda.synchronize(dev)
-        return tokens, e0.elapsed_time(e1), n_compress
+        return tokens, e0.elapsed_time(e1), n_compress, dec_bytes
 
     run(min(D, 64), False)                       # warm-up
     clocks = ClockSampler(0)
     clocks.start()
-    tokens, ms, n_compress = run(D, True)
+    tokens, ms, n_compress, dec_bytes = run(D, True)
+    hbm_peak, _, _, peak_kind = peaks()
+    achieved = dec_bytes / (ms / 1e3) / 1e9
     clk = clocks.stop()
     st = cache.check_device(sa)
     if st != snap.SNAP_OK:
@@ -729,7 +739,12 @@ def run_mixed(args):
                        "decode_steps": D, "arrival_every": every,
                        "cache": f"{wl.L_sink}+{wl.K}+{wl.L_recent}={wl.C}",
                        "output_len": "U[32,1024]", "prompt_pool": NP},
-            "decoded_tokens": tokens, "arrivals_compressed": n_compress, "clocks": clk}
+            "decoded_tokens": tokens, "arrivals_compressed": n_compress,
+            "roofline": {"bound": "hbm", "kernel": "snap_decode_step over the run (compressions overlap on a "
+                         "second stream, so this is a lower bound)", "achieved": achieved, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": peak_kind,
+                         "traffic": None, "decode_bytes": dec_bytes},
+            "clocks": clk}
     print(json.dumps(line), flush=True)
 
 
