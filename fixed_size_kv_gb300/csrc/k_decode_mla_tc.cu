@@ -78,6 +78,7 @@ enum {
 static_assert((N_BARS + 1) * 8 <= 256, "barrier area");
 static_assert(SMEM <= 232448, "shared memory");
 static_assert(TK == 64, "the mask below takes two 32-key ballots");
+static_assert(TK == MLA_KEYS, "the host plans splits and the cache tensor map in MLA_KEYS tiles");
 
 constexpr int SOFTMAX_BAR_ID = 1;           // named barrier of the softmax warps (bar 0 = __syncthreads)
 

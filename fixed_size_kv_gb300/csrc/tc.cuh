@@ -174,15 +174,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
         : "memory");
 }
-// 32 lanes x 16 consecutive 32-bit columns from registers into TMEM.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
-            taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-        : "memory");
-}
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
@@ -199,11 +190,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(a), "f"(b), "f"(c),
-                 "f"(d)
-                 : "memory");
-}
 // Asynchronous 16-byte store into another CTA's shared memory that counts its bytes
 // on that CTA's mbarrier (complete_tx): no fence or separate arrive is needed.
 __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
@@ -214,9 +200,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, floa
         "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
         : "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-    asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
-}
 // Arrive on an mbarrier in another CTA of the cluster, with the default (CTA-scope
 // release) semantics.  Used to hand a shared-memory buffer back to the peer that
 // fills it with st.async: the only ordering needed is that this CTA's reads of the
@@ -226,22 +209,6 @@ __device__ __forceinline__ void fence_acq_rel_cluster() {
 // thread, which costs about a microsecond per call.)
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
-}
-// Bulk copy (TMA engine) of `bytes` from this CTA's shared memory to shared memory of
-// a CTA of the cluster; completes `bytes` of transaction on that CTA's mbarrier.
-// Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
-                                                     uint32_t bar_cluster) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-            dst_cluster),
-        "r"(src_cta), "r"(bytes), "r"(bar_cluster)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
-// Waits until every bulk copy this thread committed has finished reading its source.
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
 }
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");

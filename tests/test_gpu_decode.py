@@ -150,7 +150,7 @@ def test_decode_compressed_equals_full_when_cache_covers():
 
 def test_decode_mla_small():
     """MLA latent layout: 576-wide keys, values = first 512 columns, 128 query heads;
-    ragged cache (C = 4 + 40 + 100, not a multiple of the 32-key tile), one sequence
+    ragged cache (C = 4 + 40 + 100, not a multiple of the 64-key tile), one sequence
     shorter than the cache, enough steps to wrap the ring."""
     wl = inputs.Workload("mla_small", 1, 128, 1, 576, 512, 4, 40, 100, 4, 5, 1, 0, 0, 0,
                          1 / math.sqrt(192))
@@ -161,7 +161,7 @@ def test_decode_mla_small():
 
 
 def test_decode_mla_long_cache_splits():
-    """MLA over a 4096-slot cache (many 32-key tiles, several splits, merge)."""
+    """MLA over a 4096-slot cache (many 64-key tiles, several splits, merge)."""
     wl = inputs.Workload("mla_mid", 1, 128, 1, 576, 512, 64, 960, 3072, 8, 7, 1, 0, 0, 0,
                          1 / math.sqrt(192))
     b = Batch(wl, [6000, 2500, 4100], [0, 1, 2], seed=13)
