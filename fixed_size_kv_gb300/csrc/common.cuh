@@ -136,6 +136,16 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic stream
+// serialization attribute may start while the previous kernel on its stream still
+// runs: pdl_wait() returns once that kernel has completed and its writes are visible
+// (at once after a normal launch), and pdl_launch_dependents() lets the next such
+// kernel start (it launches once every CTA of this grid has called it or exited).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ float bf16_round(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));
 }

@@ -16,6 +16,7 @@ namespace {
 // One CTA per sequence of the batch.  Copies the new token's rows into the ring
 // slot of position T, then advances T.
 __global__ void append_kernel(AppendArgs a) {
+    pdl_launch_dependents();    // the attention that follows may set up (it waits for this grid)
     const DevConfig& c = a.cfg;
     const int b = blockIdx.x;
     const int slot = a.slots[b];

@@ -27,6 +27,8 @@ constexpr int G_STAGE_BYTES = GQA_KEYS * G_ROWB * 2;        // K + V tile = 16 K
 constexpr int G_SMEM = G_WARPS * G_STAGES * G_STAGE_BYTES;  // 192 KB
 
 __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs a) {
+    pdl_wait();                 // the append (or whatever produced q) has completed
+    pdl_launch_dependents();    // the merge may launch once the last wave has started
     extern __shared__ __align__(1024) uint8_t smem[];
     const DevConfig& c = a.cfg;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
@@ -257,6 +259,7 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
 // One warp turns the (max, sum) pairs into weights in shared memory once; every
 // output column then reads its splits with independent loads.
 __global__ void decode_merge_kernel(DecodeArgs a) {
+    pdl_wait();                 // the attention's partials are complete and visible
     __shared__ float w_s[32];
     __shared__ float inv_l;
     const DevConfig& c = a.cfg;
@@ -303,14 +306,12 @@ cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st) {
         attr = true;
     }
     dim3 grid(a.splits, a.cfg.Hkv, a.n);
-    gqa_decode_kernel<<<grid, G_WARPS * 32, G_SMEM, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(gqa_decode_kernel, grid, dim3(G_WARPS * 32), G_SMEM, st, a);
 }
 
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st) {
     dim3 grid(a.cfg.Hq, a.n);
-    decode_merge_kernel<<<grid, 128, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(decode_merge_kernel, grid, dim3(128), 0, st, a);
 }
 
 }  // namespace snap

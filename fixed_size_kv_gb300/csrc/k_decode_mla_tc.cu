@@ -88,6 +88,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV, DecodeArgs a) {
+    pdl_wait();                 // the append (or whatever produced q) has completed
+    pdl_launch_dependents();    // the merge may launch once the last wave has started
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const DevConfig& c = a.cfg;
@@ -531,8 +533,7 @@ cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cu
         attr = true;
     }
     dim3 grid(2 * a.splits, a.n);
-    mla_decode_tc_kernel<<<grid, THREADS, SMEM, st>>>(tkv, a);
-    return cudaGetLastError();
+    return launch_dependent(mla_decode_tc_kernel, grid, dim3(THREADS), SMEM, st, tkv, a);
 }
 
 }  // namespace snap

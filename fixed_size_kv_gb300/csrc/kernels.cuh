@@ -30,6 +30,24 @@ constexpr int GQA_KEYS = 32;     // keys per warp step of the GQA decode kernel
 constexpr int MLA_KEYS = 64;     // keys per tile of the MLA decode kernel
 constexpr int MLA_HEADS = 128;   // query heads of the MLA layout (the M of its MMAs)
 
+// Launches `kernel` with programmatic stream serialization: it may start while the
+// previous kernel on `st` still runs, so its first statement must be pdl_wait().
+template <typename... Exp, typename... Act>
+cudaError_t launch_dependent(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Act&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+}
+
 cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
 // tkv: cache [max_batch][C][576], box {64, 64, 1} (queries are read from a.q directly)
 cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cudaStream_t st);
