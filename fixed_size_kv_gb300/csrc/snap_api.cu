@@ -242,20 +242,28 @@ snap_status cuda_status(cudaError_t e) {
     return SNAP_ERR_CUDA;
 }
 
-// Split count for decode: enough CTAs for whole waves of `wave` resident CTAs, never
-// more splits than tiles, and each split at least 4 tiles.
-int decode_splits(int base, int tiles, int wave) {
+// GQA decode split count.  A wave of resident CTAs streams as fast as HBM allows once
+// about 84% of the SMs read (a partial wave below that takes as long as one that
+// size), every CTA pays about one warp step of set-up and drain, and any split count
+// above one adds the merge (~3%).  The count minimises
+//   (warp steps per split + 1) x sum over waves of max(CTAs in the wave, 0.84 wave),
+// which picks one wave of ~128 CTAs at 16 x 128k (one split, no merge) and two
+// splits at 8 x 16-32k (measured on GB300 against every split count).
+int decode_splits_gqa(int base, int tiles, int wave) {
+    const int sat = (wave * 84 + 99) / 100;
     int best = 1;
-    double best_eff = 0.0;
+    double best_cost = -1.0;
     for (int s = 1; s <= MAX_DECODE_SPLITS; ++s) {
-        if (s > 1 && (tiles + s - 1) / s < 4) break;
+        const int per_split = (tiles + s - 1) / s;
+        if (s > 1 && (tiles + per_split - 1) / per_split < s) break;   // would leave a split empty
+        const int steps = (per_split + 3) / 4;                         // 4 warps, one 32-key tile each per step
         const long long ctas = (long long)base * s;
-        const long long waves = (ctas + wave - 1) / wave;
-        double eff = (double)ctas / (double)(waves * wave);
-        // prefer more parallelism until two waves are covered
-        if (ctas < 2 * wave) eff *= (double)ctas / (2.0 * wave);
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
+        const long long full = ctas / wave, rem = ctas % wave;
+        const long long units = full * wave + (rem ? (rem > sat ? rem : sat) : 0);
+        double cost = (double)(steps + 1) * (double)units;
+        if (s > 1) cost *= 1.03;
+        if (best_cost < 0.0 || cost < best_cost) {
+            best_cost = cost;
             best = s;
         }
     }
@@ -297,7 +305,7 @@ int decode_split_count(const snap_cache* cache, int n) {
     const snap_config& c = cache->cfg;
     if (c.layout == SNAP_LAYOUT_GQA) {
         const int tiles = (int)((cache->C + GQA_KEYS - 1) / GQA_KEYS);
-        return decode_splits(n * c.n_kv_heads, tiles / 4, decode_wave_ctas(cache));
+        return decode_splits_gqa(n * c.n_kv_heads, tiles, decode_wave_ctas(cache));
     }
     const int tiles = (int)((cache->C + MLA_KEYS - 1) / MLA_KEYS);
     return decode_splits_fixed_cost(2 * n, tiles, decode_wave_ctas(cache), MLA_FIXED_TILES);
