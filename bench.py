@@ -526,6 +526,13 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
         compute(sets[w])
     stream.synchronize()
     copy.synchronize()
+    # this host's pinned host->device bandwidth, on one prompt (explains the e2e number)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(copy)
+    sets[0]["K"][0].copy_(hK[0], non_blocking=True)
+    c1.record(copy)
+    copy.synchronize()
+    h2d_gbs = hK[0].numel() * 2 / (c0.elapsed_time(c1) / 1e3) / 1e9
     steps = max(1, args.steps)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -540,7 +547,8 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
     ms = reduce_max(e0.elapsed_time(e1))
     del cache
     return {"value": B * D * steps * world / (ms / 1e3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "overlap": "double-buffered inputs"}
+            "d2h_bytes_per_step": d2h, "steps": steps, "overlap": "double-buffered inputs",
+            "h2d_gbs_one_copy": h2d_gbs}
 
 
 # ----------------------------------------------------------------------------- oracle
