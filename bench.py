@@ -133,15 +133,37 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- workload
+def replica_seed(seed, rank):
+    """Each rank is an independent replica with its own inputs (weak scaling)."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(x, world, device):
+    """The slowest rank's value (timings are reported as the max over ranks)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, max_ms):
+    """Whole-job tokens per second: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (max_ms / 1e3)
+
+
 def make_batch(wl, seed, rank, device):
     import torch
     from fixed_size_kv_gb300 import inputs
-    lengths = inputs.prompt_lengths(wl, seed + 7919 * rank)
-    pre = [inputs.gen_prefill(wl, S, seed=seed + 7919 * rank, seq=b, device=device)
+    rs = replica_seed(seed, rank)
+    lengths = inputs.prompt_lengths(wl, rs)
+    pre = [inputs.gen_prefill(wl, S, seed=rs, seq=b, device=device)
            for b, S in enumerate(lengths)]
     qs, ks, vs = [], [], []
     for t in range(wl.decode_steps):
-        tok = inputs.gen_decode(wl, wl.batch, step=t, seed=seed + 7919 * rank, device=device)
+        tok = inputs.gen_decode(wl, wl.batch, step=t, seed=rs, device=device)
         qs.append(tok.q)
         ks.append(tok.k)
         vs.append(tok.v)
@@ -293,16 +315,11 @@ def run_ours(args):
         raise RuntimeError(f"device status after timed steps: {snap.status_string(st)}")
 
     def reduce_max(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(x, world, dev)
 
     total_ms = reduce_max(total_ms)
     ms_step = total_ms / args.steps
-    tokens = B * D * args.steps * world
-    value = tokens / (total_ms / 1e3)
+    value = job_throughput(B * D * args.steps, world, total_ms)
     dec_ms = reduce_max(sum(decode_ms)) / args.steps
     cmp_ms = reduce_max(sum(compress_ms)) / args.steps
     attn_avg_ms = statistics.mean(attn_ms)
