@@ -6,36 +6,31 @@
 // [latent 512 | rope 64] per cached token; the value is the latent.  The 128 heads
 // of one sequence form the M = 128 side of every MMA.
 //
-// A cluster of two CTAs handles one (sequence, split) and divides the 576 columns:
-//   rank 0 owns columns   0..255 (4 chunks of 64): its part of q.k and values 0..255
-//   rank 1 owns columns 256..575 (5 chunks):       its part of q.k and values 256..511
-// Per 64-key tile, each CTA computes its partial scores S_r = Q_r K_r^T into TMEM,
-// the two exchange their partials through distributed shared memory (both then hold
-// the same S = S_0 + S_1), run the same online softmax (same max, same rounded
-// weights), and each accumulates its half of O = P V in TMEM (256 fp32 columns).
-// No score is computed twice and each cache byte is read by one CTA only.
+// Two CTAs handle one (sequence, split) and divide the output: CTA `half` accumulates
+// O[:, 256 half .. 256 half + 255] = P V over its 256 value columns (256 fp32 TMEM
+// columns; all 512 would fill TMEM).  Each computes the whole score S = Q K^T over
+// all 576 columns itself, so the pair needs no exchange and no cluster: the scores
+// are computed twice (the cheap part of the step at this size), and the pair's two
+// reads of every cache tile start together, so the second is served by L2.
 //
-// A tcgen05.mma with a small N costs about as much as one with N = 64, so the
-// instruction count per key sets the pace: scores use N = 64 keys per MMA and P V
-// uses N = 256 (all four value chunks of the CTA in one MMA).  Operand A comes from
-// TMEM where it fits: the four latent chunks of q (rank 1's rope chunk sits in
-// shared memory) and the bf16 weights P, written over the scores they came from.
-// TMEM columns: scores / weights 0..127 (one 64-column buffer per softmax group),
-// q 128..255, this CTA's half of O 256..511.
+// Per 64-key tile: S into TMEM with N = 64 score MMAs (q's four chunks 0..3 from
+// TMEM, chunks 4..8 from shared memory), the softmax, the bf16 weights P written
+// over their scores in TMEM, then O += P V as one N = 256 MMA per 16 keys (the
+// CTA's four 64-column value chunks, 8 KB apart in the stage).  A tcgen05.mma with
+// a small N costs about as much as one with N = 64, so the instruction count per
+// key sets the pace.  TMEM columns: scores / weights 0..127 (one 64-column buffer
+// per softmax group), q 128..255, O 256..511.
 //
 // Roles (320 threads per CTA): warp 0 issues TMA loads (and L2 prefetches ahead),
 // warp 1 owns TMEM and one thread issues tcgen05.mma from two queues (scores of the
-// next tile, P V of the oldest ready tile).  Warps 2..9 run the softmax as two
+// next tile, P V of the oldest tile with weights), warps 2..9 run the softmax as two
 // groups of four warps (one TMEM lane quarter each; thread = head) that take
-// alternate tiles, so two tiles are in the softmax at once: while one group waits
-// for the peer's partial scores, the other computes weights.
-//
-// Both groups accumulate into the one O in TMEM, so they share one running max.
-// It is handed from the group of tile i-1 to the group of tile i (per lane
-// quarter, through an mbarrier) and moves lazily: only when a tile's max exceeds it
-// by more than 32 in log2 units, and then O is rescaled in TMEM after P V of the
-// previous tile.  Each group keeps its own sum of weights, rescaled whenever the
-// shared max moves; the two sums are added at the end.  Every wait is bounded.
+// alternate tiles.  Both groups accumulate into the one O, so they share one running
+// max, handed from the group of tile i-1 to the group of tile i (per lane quarter,
+// through an mbarrier).  It moves lazily: only when a tile's max exceeds it by more
+// than 32 in log2 units, and then O is rescaled in TMEM after P V of the previous
+// tile.  Each group keeps its own sum of weights, rescaled when the shared max
+// moves; the two sums are added at the end.  Every wait is bounded.
 #include "kernels.cuh"
 #include "tc.cuh"
 
@@ -47,20 +42,19 @@ constexpr float NEG_INF = -__builtin_huge_valf();
 constexpr int MV = 512;                     // value (latent) width
 constexpr int HEADS = 128;                  // M of every MMA
 constexpr int TK = 64;                      // keys per tile
+constexpr int NCH = 9;                      // 64-column chunks of a key row (8 latent + rope)
+constexpr int QT_CH = 4;                    // chunks of q held in TMEM (the rest in shared memory)
 constexpr int CH_B = TK * 128;              // one 64-column chunk of a KV tile: 8 KB
-constexpr int MAXCH = 5;                    // chunks owned by rank 1
-constexpr int KST = 3;                      // KV tile stages
+constexpr int QCH_B = HEADS * 128;          // one 64-column chunk of q: 16 KB
+constexpr int KST = 2;                      // KV tile stages (L2 prefetch runs further ahead)
 constexpr int NG = 2;                       // softmax groups (tile i goes to group i % 2)
 constexpr int THREADS = 64 + NG * 128;
 constexpr float RESCALE_GAP = 32.f;         // weights up to 2^32 stay exact in fp32 O and l
-constexpr int XROW_B = TK * 4;              // one head's partial scores: 256 B
-constexpr int XBUF_B = HEADS * XROW_B;      // one tile's partial scores: 32 KB
 
-constexpr int OFF_KV = 0;
-constexpr int OFF_QR = OFF_KV + KST * MAXCH * CH_B;       // 120 KB
-constexpr int OFF_X = OFF_QR + HEADS * 128;               // + 16 KB (rank 1's rope chunk of q)
-constexpr int OFF_ML = OFF_X + NG * XBUF_B;               // + 64 KB (incoming partial scores, per group)
-constexpr int OFF_BAR = OFF_ML + 1536;                    // + running max [128] and group sums [2][128]
+constexpr int OFF_Q = 0;                                  // q chunks 4..8: 80 KB
+constexpr int OFF_KV = OFF_Q + (NCH - QT_CH) * QCH_B;     // + KST x 72 KB
+constexpr int OFF_ML = OFF_KV + KST * NCH * CH_B;         // running max [128] and group sums [2][128]
+constexpr int OFF_BAR = OFF_ML + 1536;
 constexpr int SMEM = OFF_BAR + 256 + 1024;                // barriers + alignment slack
 
 enum {
@@ -70,10 +64,8 @@ enum {
     B_S_FULL = 1 + 2 * KST,      // + NG: scores of the group's tile are in TMEM
     B_SP_EMPTY = 3 + 2 * KST,    // + NG: P V of the group's previous tile done (buffer free)
     B_P_FULL = 5 + 2 * KST,      // + NG: weights of the group's tile are in TMEM
-    B_X_FULL = 7 + 2 * KST,      // + NG
-    B_X_EMPTY = 9 + 2 * KST,     // + NG
-    B_M_READY = 11 + 2 * KST,    // + 4 (one per lane quarter)
-    N_BARS = 15 + 2 * KST
+    B_M_READY = 7 + 2 * KST,     // + 4 (one per lane quarter)
+    N_BARS = 11 + 2 * KST
 };
 static_assert((N_BARS + 1) * 8 <= 256, "barrier area");
 static_assert(SMEM <= 232448, "shared memory");
@@ -86,22 +78,19 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return mbar_wait_bounded(bar, parity, abort_flag);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 1)
     mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV, DecodeArgs a) {
     pdl_wait();                 // the append (or whatever produced q) has completed
     pdl_launch_dependents();    // the merge may launch once the last wave has started
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const DevConfig& c = a.cfg;
-    const uint32_t rank = cluster_rank();
-    const uint32_t peer = rank ^ 1u;
+    const int half = blockIdx.x & 1;            // which 256 value columns this CTA accumulates
     const int split = blockIdx.x >> 1, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nch = rank == 0 ? 4 : 5;          // chunks owned (the last of rank 1's is the rope)
-    const int c0 = rank == 0 ? 0 : 4;           // first owned chunk
 
     const uint32_t s_base = smem_u32(smem);
-    const uint32_t s_kv = s_base + OFF_KV, s_qr = s_base + OFF_QR, s_x = s_base + OFF_X;
+    const uint32_t s_q = s_base + OFF_Q, s_kv = s_base + OFF_KV;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     auto bar = [&](int i) { return smem_u32(bars + i); };
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + N_BARS);
@@ -122,8 +111,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             mbar_init(bar(B_S_FULL + g), 1);
             mbar_init(bar(B_SP_EMPTY + g), 1);
             mbar_init(bar(B_P_FULL + g), 4);
-            mbar_init(bar(B_X_FULL + g), 1);    // this CTA's expect_tx + the peer's st.async bytes
-            mbar_init(bar(B_X_EMPTY + g), 4);   // the peer's four warps of group g
         }
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_M_READY + q), 1);
         *abort_flag = 0;
@@ -134,17 +121,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tmem_relinquish();
     }
     __syncthreads();
-    cluster_sync_all();                 // both CTAs' barriers exist before any remote arrive
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    // TMEM: scores, then weights (one 64-column buffer per group), q, O
+    // TMEM: scores, then weights (one 64-column buffer per group), q chunks 0..3, O
     const uint32_t T_S = tmem, T_Q = tmem + 128, T_O = tmem + 256;
 
-    // status detail: 300 + rank, the wait that gave up, the tile index reached
+    // status detail: 300 + half, the wait that gave up, the tile index reached
     int cur_tile = -1;
     auto fail = [&](int role) {
         *abort_flag = 1;
-        report_error(a.status, SNAP_ERR_TIMEOUT, 300 + (int)rank, role, cur_tile);
+        report_error(a.status, SNAP_ERR_TIMEOUT, 300 + half, role, cur_tile);
     };
 
     SlotValidity sv;
@@ -152,7 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     if (slot_ok) {
         m = a.meta[slot];
         sv.init(m, c);
-    } else if (threadIdx.x == 0 && split == 0 && rank == 0) {
+    } else if (threadIdx.x == 0 && split == 0 && half == 0) {
         report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
     }
     const int ntiles = (c.C + TK - 1) / TK;
@@ -169,68 +155,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             tma_prefetch(&tmKV);
             constexpr int AHEAD = 4;    // tiles on their way to L2 ahead of the loads
             for (int t = t_begin; t < min(t_end, t_begin + AHEAD); ++t)
-                for (int j = 0; j < nch; ++j) tma_prefetch_3d(&tmKV, 64 * (c0 + j), t * TK, slot);
+                for (int j = 0; j < NCH; ++j) tma_prefetch_3d(&tmKV, 64 * j, t * TK, slot);
             int i = 0;
             for (int t = next_tile(t_begin); t < t_end; t = next_tile(t + 1), ++i) {
                 cur_tile = t;
                 if (t + AHEAD < t_end)
-                    for (int j = 0; j < nch; ++j) tma_prefetch_3d(&tmKV, 64 * (c0 + j), (t + AHEAD) * TK, slot);
+                    for (int j = 0; j < NCH; ++j) tma_prefetch_3d(&tmKV, 64 * j, (t + AHEAD) * TK, slot);
                 const int st = i % KST;
                 const uint32_t n = i / KST;
                 if (!wait_bar(bar(B_KV_EMPTY + st), (n & 1) ^ 1, abort_flag)) { fail(0); break; }
-                mbar_expect_tx(bar(B_KV_FULL + st), nch * CH_B);
-                for (int j = 0; j < nch; ++j)
-                    tma_load_3d(s_kv + (st * MAXCH + j) * CH_B, &tmKV, bar(B_KV_FULL + st), 64 * (c0 + j), t * TK,
-                                slot);
+                mbar_expect_tx(bar(B_KV_FULL + st), NCH * CH_B);
+                for (int j = 0; j < NCH; ++j)
+                    tma_load_3d(s_kv + (st * NCH + j) * CH_B, &tmKV, bar(B_KV_FULL + st), 64 * j, t * TK, slot);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && t_begin < t_end) {
             const uint32_t id_qk = idesc_bf16(HEADS, TK);
-            const uint32_t id_pv = idesc_bf16_bmn(HEADS, 256);   // all four value chunks per MMA
+            const uint32_t id_pv = idesc_bf16_bmn(HEADS, 256);   // this CTA's four value chunks per MMA
             bool ok = wait_bar(bar(B_Q_FULL), 0, abort_flag);
             if (!ok) fail(10);
-            // Two queues: the scores of the next tile (needs its KV and its group's
-            // buffer back from P V two tiles ago) and P V of the oldest tile with
-            // weights ready.  Issue whichever is ready.
+            // Two queues: P V of the oldest tile with weights ready (first: it frees a
+            // KV stage for the next load), else the scores of the next tile (needs its
+            // KV and its group's buffer back from P V two tiles ago).
             int n_t = 0;
             for (int t = next_tile(t_begin); t < t_end; t = next_tile(t + 1)) ++n_t;
             int qk = 0, pv = 0;
             uint64_t t_idle = 0;
             while (ok && pv < n_t) {
                 bool progressed = false;
-                if (qk < n_t && mbar_test_wait(bar(B_SP_EMPTY + (qk & 1)), ((qk >> 1) & 1) ^ 1) &&
-                    mbar_test_wait(bar(B_KV_FULL + qk % KST), (qk / KST) & 1)) {
-                    tc_fence_after();
-                    const int st = qk % KST, sb = qk & 1;
-                    const uint32_t d = T_S + sb * TK;
-                    for (int j = 0; j < 4; ++j)         // latent chunks: q from TMEM
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)     // 16 columns (8 TMEM columns of q) per step
-                            tc_mma_ta(d, T_Q + j * 32 + k * 8, desc_sw128(s_kv + (st * MAXCH + j) * CH_B + k * 32),
-                                      id_qk, (j | k) ? 1u : 0u);
-                    if (nch == 5)                       // rank 1's rope chunk: q from shared memory
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc_mma(d, desc_sw128(s_qr + k * 32), desc_sw128(s_kv + (st * MAXCH + 4) * CH_B + k * 32),
-                                   id_qk, 1u);
-                    tc_commit(bar(B_S_FULL + sb));
-                    ++qk;
-                    progressed = true;
-                }
                 if (pv < qk && mbar_test_wait(bar(B_P_FULL + (pv & 1)), (pv >> 1) & 1)) {
                     tc_fence_after();
                     const int stp = pv % KST;
                     const uint32_t pa = T_S + (pv & 1) * TK;  // the weights, written over the scores
-                    // N = 256: this CTA's four 64-column value chunks (CH_B apart) in one MMA
+                    const uint32_t vb = s_kv + (stp * NCH + 4 * half) * CH_B;
 #pragma unroll
                     for (int k = 0; k < TK / 16; ++k)       // 16 keys (8 TMEM columns of P) per step
-                        tc_mma_ta(T_O, pa + k * 8, desc_sw128_mn(s_kv + stp * MAXCH * CH_B + k * 2048, CH_B), id_pv,
+                        tc_mma_ta(T_O, pa + k * 8, desc_sw128_mn(vb + k * 2048, CH_B), id_pv,
                                   (pv > 0 || k > 0) ? 1u : 0u);
                     tc_commit(bar(B_SP_EMPTY + (pv & 1)));
                     tc_commit(bar(B_KV_EMPTY + stp));
                     ++pv;
+                    progressed = true;
+                }
+                if (!progressed && qk < n_t && mbar_test_wait(bar(B_SP_EMPTY + (qk & 1)), ((qk >> 1) & 1) ^ 1) &&
+                    mbar_test_wait(bar(B_KV_FULL + qk % KST), (qk / KST) & 1)) {
+                    tc_fence_after();
+                    const int st = qk % KST, sb = qk & 1;
+                    const uint32_t d = T_S + sb * TK;
+                    for (int j = 0; j < QT_CH; ++j)     // q chunks 0..3 from TMEM
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)     // 16 columns (8 TMEM columns of q) per step
+                            tc_mma_ta(d, T_Q + j * 32 + k * 8, desc_sw128(s_kv + (st * NCH + j) * CH_B + k * 32),
+                                      id_qk, (j | k) ? 1u : 0u);
+                    for (int j = QT_CH; j < NCH; ++j)   // q chunks 4..8 from shared memory
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma(d, desc_sw128(s_q + (j - QT_CH) * QCH_B + k * 32),
+                                   desc_sw128(s_kv + (st * NCH + j) * CH_B + k * 32), id_qk, 1u);
+                    tc_commit(bar(B_S_FULL + sb));
+                    ++qk;
                     progressed = true;
                 }
                 if (progressed) {
@@ -255,58 +240,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         const uint32_t m_ready = bar(B_M_READY + quarter);
         bool ok = true;
 
-        // q: the latent chunks of this CTA into TMEM (one head per lane, the two groups
-        // take alternate chunks), rank 1's rope chunk into shared memory as a 128-byte
-        // swizzled K-major tile (group 1 writes it).
+        // q: chunks 0..3 into TMEM (one head per lane), chunks 4..8 into shared memory as
+        // 128-byte swizzled K-major tiles; the two groups take alternate chunks.
         {
-            const bf16* qrow = a.q + ((size_t)b * c.Hq + row) * (size_t)c.dqk + 64 * c0;
-            for (int j = g; j < 4; j += NG) {
+            const bf16* qrow = a.q + ((size_t)b * c.Hq + row) * (size_t)c.dqk;
+            for (int j = g; j < NCH; j += NG) {
                 const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * j);
-                float v[32];
+                if (j < QT_CH) {
+                    float v[32];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint4 u = src[e];
-                    v[4 * e] = __uint_as_float(u.x);
-                    v[4 * e + 1] = __uint_as_float(u.y);
-                    v[4 * e + 2] = __uint_as_float(u.z);
-                    v[4 * e + 3] = __uint_as_float(u.w);
-                }
-                tmem_st32(T_Q + lane_off + 32 * j, v);
-            }
-            if (nch == 5 && g == 1) {
-                const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * 4);
-                const uint32_t dst = s_qr + (row >> 3) * 1024 + (row & 7) * 128;
+                    for (int e = 0; e < 8; ++e) {
+                        const uint4 u = src[e];
+                        v[4 * e] = __uint_as_float(u.x);
+                        v[4 * e + 1] = __uint_as_float(u.y);
+                        v[4 * e + 2] = __uint_as_float(u.z);
+                        v[4 * e + 3] = __uint_as_float(u.w);
+                    }
+                    tmem_st32(T_Q + lane_off + 32 * j, v);
+                } else {
+                    const uint32_t dst = s_q + (j - QT_CH) * QCH_B + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint4 u = src[e];
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + ((e ^ (row & 7)) << 4)),
-                                 "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w)
-                                 : "memory");
+                    for (int e = 0; e < 8; ++e) {
+                        const uint4 u = src[e];
+                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + ((e ^ (row & 7)) << 4)),
+                                     "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w)
+                                     : "memory");
+                    }
                 }
-                fence_proxy_async();
             }
+            fence_proxy_async();
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_Q_FULL));
         }
-
-        // Sends tile j's partial scores (in registers) into the peer's exchange buffer
-        // of this group with st.async; the 16-byte chunks of a 256-byte row are
-        // XOR-swizzled by row so that a warp reading chunk k of 32 rows spreads over
-        // the banks.
-        auto send = [&](int j, const float (&s)[TK]) -> bool {
-            // the peer has consumed what this group sent for its previous tile
-            if (!__all_sync(0xffffffffu, wait_bar(bar(B_X_EMPTY + g), ((j >> 1) & 1) ^ 1, abort_flag))) return false;
-            // the peer's scores of tile j will land in this group's buffer: announce the bytes
-            if (quarter == 0 && lane == 0) mbar_expect_tx(bar(B_X_FULL + g), XBUF_B);
-            const uint32_t dst = mapa(s_x + g * XBUF_B + row * XROW_B, peer);
-            const uint32_t xfull_peer = mapa(bar(B_X_FULL + g), peer);
-#pragma unroll
-            for (int k = 0; k < TK / 4; ++k)
-                st_async_v4(dst + 16 * (k ^ (row & 7)), s[4 * k], s[4 * k + 1], s[4 * k + 2], s[4 * k + 3], xfull_peer);
-            return true;
-        };
 
         float m_used = NEG_INF;     // the running max this group's sum l_g is relative to
         float l_g = 0.f;
@@ -315,7 +282,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             if ((i & 1) != g || !ok) continue;
             cur_tile = t;
             const int k_g = i >> 1;             // this group's k-th tile: barrier phase parity k_g & 1
-            // 1. this CTA's partial scores of tile i, out of TMEM
+            // 1. the scores of tile i, out of TMEM
             float s[TK];
             if (!__all_sync(0xffffffffu, wait_bar(bar(B_S_FULL + g), k_g & 1, abort_flag))) {
                 fail(3);
@@ -335,31 +302,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     s[32 + k] = hi[k];
                 }
             }
-            // 2. to the peer
-            if (!send(i, s)) {
-                fail(6);
-                ok = false;
-                continue;
-            }
-            // 3. the peer's partial scores of this tile
-            if (!__all_sync(0xffffffffu, wait_bar(bar(B_X_FULL + g), k_g & 1, abort_flag))) {
-                fail(4);
-                ok = false;
-                continue;
-            }
-            const float4* xr = reinterpret_cast<const float4*>(smem + OFF_X + g * XBUF_B + row * XROW_B);
-#pragma unroll
-            for (int k = 0; k < TK / 4; ++k) {
-                const float4 v = xr[k ^ (row & 7)];
-                // rank 0 adds S_0 + S_1 and rank 1 S_1 + S_0: the same value in both CTAs
-                s[4 * k] += v.x;
-                s[4 * k + 1] += v.y;
-                s[4 * k + 2] += v.z;
-                s[4 * k + 3] += v.w;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(mapa(bar(B_X_EMPTY + g), peer));
-            // 4. mask (two ballots for the tile's 64 slots), scale, tile max
+            // 2. mask (two ballots for the tile's 64 slots), scale, tile max
             const uint32_t v0 = __ballot_sync(0xffffffffu, t * TK + lane < c.C && sv.valid(t * TK + lane));
             const uint32_t v1 =
                 __ballot_sync(0xffffffffu, t * TK + 32 + lane < c.C && sv.valid(t * TK + 32 + lane));
@@ -370,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 s[32 + k] = ((v1 >> k) & 1u) ? s[32 + k] * sl2 : NEG_INF;
                 mt = fmaxf(mt, fmaxf(s[k], s[32 + k]));
             }
-            // 5. the running max as left by tile i-1 (the other group)
+            // 3. the running max as left by tile i-1 (the other group)
             float m_prev = NEG_INF;
             if (i > 0) {
                 if (!__all_sync(0xffffffffu, wait_bar(m_ready, (i - 1) & 1, abort_flag))) {
@@ -411,7 +354,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 tmem_st_wait();
                 tc_fence_before();
             }
-            // 6. hand the running max to tile i+1
+            // 4. hand the running max to tile i+1
             m_sh[row] = m_new;
             __syncwarp();
             if (lane == 0) mbar_arrive(m_ready);
@@ -419,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 l_g = m_used == NEG_INF ? l_g : l_g * ex2(m_used - m_new);
                 m_used = m_new;
             }
-            // 7. weights (bf16, two keys per TMEM column) over this group's scores (read
+            // 5. weights (bf16, two keys per TMEM column) over this group's scores (read
             //    above, so the buffer is free until P V of this tile releases it)
             float w[32];
             float psum = 0.f;
@@ -439,7 +382,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         }
         const int n_t = i;
 
-        // 8. the final running max (from the group of the last tile) and P V of the
+        // 6. the final running max (from the group of the last tile) and P V of the
         //    last tile done (its commit covers every earlier MMA too)
         float m_fin = NEG_INF;
         if (ok && n_t > 0) {
@@ -461,10 +404,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         asm volatile("bar.sync %0, %1;\n" ::"n"(SOFTMAX_BAR_ID), "n"(NG * 128) : "memory");
         const float l_run = l_sh[row] + l_sh[HEADS + row];
 
-        // 9. this CTA's half of the output; group g writes TMEM columns 128 g .. 128 g + 127
+        // 7. this CTA's half of the output; group g writes TMEM columns 128 g .. 128 g + 127
         if (ok && row < c.Hq) {
             const int head = row;
-            const int d0 = rank == 0 ? 0 : 256;
+            const int d0 = 256 * half;
             for (int j = 4 * g; j < 4 * g + 4; ++j) {
                 float o[32];
                 if (n_t > 0) {
@@ -488,7 +431,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                     *reinterpret_cast<float4*>(dst + e) =
                         make_float4(o[e] * scale, o[e + 1] * scale, o[e + 2] * scale, o[e + 3] * scale);
             }
-            if (a.splits > 1 && rank == 0 && g == 0) {
+            if (a.splits > 1 && half == 0 && g == 0) {
                 const size_t pi = ((size_t)b * a.splits + split) * c.Hq + head;
                 a.part_ml[pi * 2 + 0] = m_fin;
                 a.part_ml[pi * 2 + 1] = l_run;
@@ -497,7 +440,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
 
     __syncthreads();
-    cluster_sync_all();                 // no CTA leaves while its peer may still write to it
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -513,16 +455,12 @@ int mla_decode_wave_ctas() {
     if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
     if (cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
         return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, (const void*)mla_decode_tc_kernel, &cfg) != cudaSuccess ||
-        clusters <= 0)
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mla_decode_tc_kernel, THREADS, SMEM) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per_sm <= 0)
         return 0;
-    if (dev >= 0 && dev < 64) cached[dev] = 2 * clusters;
-    return 2 * clusters;
+    if (dev >= 0 && dev < 64) cached[dev] = per_sm * sms;
+    return per_sm * sms;
 }
 
 cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cudaStream_t st) {

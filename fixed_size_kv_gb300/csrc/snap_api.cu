@@ -270,7 +270,7 @@ int decode_splits_gqa(int base, int tiles, int wave) {
     return best;
 }
 
-// MLA decode: each CTA also pays a fixed cost (TMEM and cluster setup, the q load,
+// MLA decode: each CTA also pays a fixed cost (TMEM setup, the q load,
 // writing its partial output) worth about this many 64-key tiles, so its split
 // count minimises waves x (tiles per split + that cost) instead.
 constexpr int MLA_FIXED_TILES = 8;
@@ -292,7 +292,7 @@ int decode_splits_fixed_cost(int base, int tiles, int wave, int fixed_tiles) {
 }
 
 // CTAs of one decode-attention kernel resident at once: one per SM for GQA; for MLA
-// two per co-resident cluster (the GPCs may leave SMs that cannot host a pair).
+// as many as the occupancy query reports (one per SM).
 int decode_wave_ctas(const snap_cache* cache) {
     if (cache->cfg.layout == SNAP_LAYOUT_GQA) return num_sms();
     const int w = mla_decode_wave_ctas();
