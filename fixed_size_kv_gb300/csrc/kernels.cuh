@@ -52,7 +52,7 @@ cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
 // tkv: cache [max_batch][C][576], box {64, 64, 1} (queries are read from a.q directly)
 cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cudaStream_t st);
 // CTAs of the MLA decode kernel that can be resident at once on the current device
-// (two per co-resident cluster; 0 if the occupancy query fails).
+// (one per SM at its shared-memory size; 0 if the occupancy query fails).
 int mla_decode_wave_ctas();
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st);
 

@@ -178,42 +178,6 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
-// --------------------------------------------------------- clusters / DSMEM
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-    return r;
-}
-// Address of the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
-    return r;
-}
-// Asynchronous 16-byte store into another CTA's shared memory that counts its bytes
-// on that CTA's mbarrier (complete_tx): no fence or separate arrive is needed.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
-                                            uint32_t cluster_bar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(
-            cluster_addr),
-        "f"(a), "f"(b), "f"(c), "f"(d), "r"(cluster_bar)
-        : "memory");
-}
-// Arrive on an mbarrier in another CTA of the cluster, with the default (CTA-scope
-// release) semantics.  Used to hand a shared-memory buffer back to the peer that
-// fills it with st.async: the only ordering needed is that this CTA's reads of the
-// buffer come first, and the peer's bytes become visible here through the
-// complete_tx of the buffer's own mbarrier, not through this arrive.  (A
-// cluster-scope release would wait for every outstanding memory operation of the
-// thread, which costs about a microsecond per call.)
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
 // Shared-memory matrix descriptor of a K-major bf16 tile stored as TMA writes it
 // with 128-byte swizzling: rows of 64 elements (128 B), 8-row groups 1024 B apart.
 // The tile base must be 1024-byte aligned; advancing along K inside the 64-element
