@@ -285,13 +285,24 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
     }
     __syncthreads();
     const float il = inv_l;
-    for (int d = threadIdx.x; d < c.dv; d += blockDim.x) {
-        float O = 0.f;
+    // four output columns per thread (d_v is 128 or 512): every split's load of a
+    // thread is in flight at once
+    const int dv4 = c.dv / 4;
+    for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x) {
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         if (il != 0.f) {
 #pragma unroll 8
-            for (int s = 0; s < a.splits; ++s) O += w_s[s] * a.part_o[((p0 + s) * c.G + hh) * c.dv + d];
+            for (int s = 0; s < a.splits; ++s) {
+                const float4 v = reinterpret_cast<const float4*>(a.part_o + ((p0 + s) * c.G + hh) * c.dv)[d4];
+                const float w = w_s[s];
+                O.x += w * v.x;
+                O.y += w * v.y;
+                O.z += w * v.z;
+                O.w += w * v.w;
+            }
         }
-        a.out[((size_t)b * c.Hq + i) * c.dv + d] = O * il;
+        reinterpret_cast<float4*>(a.out + ((size_t)b * c.Hq + i) * c.dv)[d4] =
+            make_float4(O.x * il, O.y * il, O.z * il, O.w * il);
     }
 }
 
@@ -311,7 +322,8 @@ cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st) {
 
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st) {
     dim3 grid(a.cfg.Hq, a.n);
-    return launch_dependent(decode_merge_kernel, grid, dim3(128), 0, st, a);
+    const int threads = a.cfg.dv / 4 < 32 ? 32 : (a.cfg.dv / 4 > 128 ? 128 : a.cfg.dv / 4);   // one float4 each
+    return launch_dependent(decode_merge_kernel, grid, dim3(threads), 0, st, a);
 }
 
 }  // namespace snap
