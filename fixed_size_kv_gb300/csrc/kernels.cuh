@@ -55,6 +55,8 @@ cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cu
 // (one per SM at its shared-memory size; 0 if the occupancy query fails).
 int mla_decode_wave_ctas();
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st);
+// One kernel whose only (bounded) wait can never be satisfied: records SNAP_ERR_TIMEOUT.
+cudaError_t launch_bounded_wait_selftest(int32_t* status, cudaStream_t st);
 
 // ----------------------------------------------------------------- append
 struct AppendArgs {

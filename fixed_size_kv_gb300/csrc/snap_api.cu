@@ -635,6 +635,11 @@ snap_status snap_decode_step(snap_cache* cache, const int32_t* slots, int n, con
     return s != SNAP_OK ? s : snap_decode_attn(cache, slots, n, q, out, ws, ws_bytes, stream);
 }
 
+snap_status snap_selftest_bounded_wait(snap_cache* cache, void* stream) {
+    if (!cache) return SNAP_ERR_INVALID_ARG;
+    return cuda_status(launch_bounded_wait_selftest(cache->status, static_cast<cudaStream_t>(stream)));
+}
+
 snap_status snap_check_device(snap_cache* cache, void* stream) {
     if (!cache) return SNAP_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -63,6 +63,7 @@ SIGNATURES = {
     "snap_decode_append": (_I, [_VP, _VP, _I, _VP, _VP, _VP]),
     "snap_decode_attn_ws_bytes": (_I, [_P(snap_config), _I, _P(_SZ)]),
     "snap_decode_attn_plan": (_I, [_VP, _I, _P(_I), _P(_I), _P(_I)]),
+    "snap_selftest_bounded_wait": (_I, [_VP, _VP]),
     "snap_decode_attn": (_I, [_VP, _VP, _I, _VP, _VP, _VP, _SZ, _VP]),
     "snap_decode_step": (_I, [_VP, _VP, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "snap_check_device": (_I, [_VP, _VP]),
@@ -280,6 +281,11 @@ class SnapCache:
         _check(load().snap_decode_attn_plan(self.handle, n, ctypes.byref(sp), ctypes.byref(tp), ctypes.byref(wv)),
                "snap_decode_attn_plan")
         return sp.value, tp.value, wv.value
+
+    def selftest_bounded_wait(self, stream=None) -> None:
+        """snap_selftest_bounded_wait: one kernel whose only wait expires (about 2 s); the
+        next check_device() returns SNAP_ERR_TIMEOUT."""
+        _check(load().snap_selftest_bounded_wait(self.handle, _stream(stream)), "snap_selftest_bounded_wait")
 
     def check_device(self, stream=None) -> int:
         return load().snap_check_device(self.handle, _stream(stream))

@@ -234,6 +234,16 @@ snap_status snap_decode_step(snap_cache* cache, const int32_t* slots, int n, con
 snap_status snap_check_device(snap_cache* cache, void* stream);
 
 /*
+ * Self-test of the error path that every kernel's bounded waits share: launches one
+ * kernel whose single wait can never be satisfied (an mbarrier that nothing arrives
+ * on).  The wait gives up after its bound (about 2 s of the device's global timer) and
+ * the kernel records SNAP_ERR_TIMEOUT (detail 900) in the cache's status word, which
+ * the next snap_check_device() returns.  Nothing faults or hangs; the device context
+ * stays usable.  SNAP_ERR_INVALID_ARG for a null cache.
+ */
+snap_status snap_selftest_bounded_wait(snap_cache* cache, void* stream);
+
+/*
  * Bytes of device scratch that snap_decode_attn_noalloc() draws on (32 MiB).  The
  * array is part of the library's device image: every GPU that loads libsnap holds
  * it until the process exits.
