@@ -198,3 +198,67 @@ def test_decode_plan_covers_every_tile(mla):
         splits, per, wave = cache.decode_attn_plan(n)
         assert 1 <= splits <= 32 and wave >= 1
         assert splits * per >= tiles and (splits - 1) * per < tiles
+
+
+def test_graph_replayed_decode_steps_match_oracle():
+    """The benchmark's launch form: snap_decode_step (append, attention with
+    programmatic dependent launch, merge) for several steps captured once as a CUDA
+    graph and replayed; every step's output against the oracle."""
+    wl = inputs.Workload("graph", 0, 32, 8, 128, 128, 4, 2044, 2048, 16, 7, 4, 0, 0, 0, 1 / math.sqrt(128))
+    b = Batch(wl, [6000, 300, 2100, 4500], slots=[0, 1, 2, 3], seed=23, max_batch=4)
+    b.step(0, fused=True)            # one eager step first (one-time launch set-up), as the bench warms up
+    steps = 6
+    toks = [inputs.gen_decode(wl, 4, step=1 + t, seed=23) for t in range(steps)]
+    q = [t.q.cuda() for t in toks]
+    k = [t.k.cuda() for t in toks]
+    v = [t.v.cuda() for t in toks]
+    outs = [torch.empty((4, wl.n_q_heads, wl.d_v), dtype=torch.float32, device="cuda") for _ in range(steps)]
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for t in range(steps):
+            b.cache.decode_step(b.dslots, q[t], k[t], v[t], out=outs[t], stream=stream)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    stream.synchronize()
+    assert b.cache.check_device() == snap.SNAP_OK
+    for t in range(steps):
+        for i in range(4):
+            oracle.append(b.ocaches[i], toks[t].k[i], toks[t].v[i])
+            check_outputs(outs[t][i], oracle.decode_attn(b.ocaches[i], toks[t].q[i]), f"graph step {t} seq {i}")
+
+
+def test_compress_on_second_stream_while_decoding():
+    """The mixed workload's lifecycle: a new request is compressed into a free slot on a
+    second stream while the other slots keep decoding on the first; afterwards all of
+    them decode together.  Every output against the oracle."""
+    wl = inputs.Workload("mix", 0, 32, 8, 128, 128, 4, 1020, 1024, 16, 7, 4, 0, 0, 0, 1 / math.sqrt(128))
+    b = Batch(wl, [3000, 1500, 2500], slots=[0, 1, 2], seed=29, max_batch=4)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    sa.wait_stream(torch.cuda.current_stream())
+    sb.wait_stream(torch.cuda.current_stream())
+    new = inputs.gen_prefill(wl, 2800, seed=29, seq=9)
+    nK, nV, nQ = new.K.cuda(), new.V.cuda(), new.Q.cuda()
+    torch.cuda.synchronize()
+    b.cache.compress(3, nK, nV, nQ, stream=sb)                 # the arrival, on stream B
+    for t in range(8):                                         # the others decode on stream A
+        tok = inputs.gen_decode(wl, 3, step=t, seed=29)
+        out = b.cache.decode_step(b.dslots, tok.q.cuda(), tok.k.cuda(), tok.v.cuda(), stream=sa)
+        sa.synchronize()
+        for i in range(3):
+            oracle.append(b.ocaches[i], tok.k[i], tok.v[i])
+            check_outputs(out[i], oracle.decode_attn(b.ocaches[i], tok.q[i]), f"while compressing, step {t} seq {i}")
+    sb.synchronize()
+    assert b.cache.check_device() == snap.SNAP_OK
+    onew = oracle.compress(oracle_cfg(wl), new.K, new.V, new.Q)
+    slots = torch.tensor([0, 1, 2, 3], dtype=torch.int32, device="cuda")
+    ocs = b.ocaches + [onew]
+    for t in range(8, 12):                                     # the arrival has joined the batch
+        tok = inputs.gen_decode(wl, 4, step=t, seed=29)
+        out = b.cache.decode_step(slots, tok.q.cuda(), tok.k.cuda(), tok.v.cuda())
+        torch.cuda.synchronize()
+        for i in range(4):
+            oracle.append(ocs[i], tok.k[i], tok.v[i])
+            check_outputs(out[i], oracle.decode_attn(ocs[i], tok.q[i]), f"joined, step {t} seq {i}")
+    assert b.cache.check_device() == snap.SNAP_OK
