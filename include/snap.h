@@ -58,11 +58,11 @@ enum { SNAP_LAYOUT_GQA = 0, SNAP_LAYOUT_MLA = 1 };
  * Cache configuration.
  *  layout      SNAP_LAYOUT_GQA: separate K and V, n_q_heads / n_kv_heads query heads per
  *              KV head (query head i reads KV head i / G).  Supported: d_qk == d_v == 128,
- *              G = n_q_heads / n_kv_heads <= 8.
+ *              G = n_q_heads / n_kv_heads in {1, 2, 4, 8}.
  *              SNAP_LAYOUT_MLA: one latent KV head (n_kv_heads == 1); the key row is
  *              [latent (d_v) | rope (d_qk - d_v)] and the value is its first d_v columns
  *              (absorbed-query attention, DeepSeek-V2 style).  Supported: d_qk == 576,
- *              d_v == 512, n_q_heads a multiple of 16.
+ *              d_v == 512, n_q_heads == 128 (the M side of the decode MMAs).
  *  L_sink, K, L_recent   segment sizes; C = L_sink + K + L_recent slots per KV head.
  *  W           observation window (last W prompt queries); 1 <= W <= L_recent.
  *  P           max-pool kernel width, odd, >= 1.
@@ -195,8 +195,9 @@ snap_status snap_decode_attn_ws_bytes(const snap_config* cfg, int max_n, size_t*
 /*
  * The launch plan snap_decode_attn() uses for a batch of n sequences on the current
  * device: *splits key ranges per sequence (merged at the end when > 1), each walking
- * *tiles_per_split key tiles (32 keys), and *ctas_per_wave CTAs of the attention
- * kernel resident at once.  Host-side only (no kernel runs); for profiling and
+ * *tiles_per_split key tiles (32 keys for GQA, 64 for MLA), and *ctas_per_wave CTAs of
+ * the attention kernel resident at once.  The split count follows a cost model of the
+ * kernels measured on GB300 (one wave of ~128 CTAs at 16 x 128k GQA, no merge).  Host-side only (no kernel runs); for profiling and
  * capacity planning.  SNAP_ERR_INVALID_ARG for a null pointer or n < 1,
  * SNAP_ERR_CUDA when no device is current.
  */
@@ -266,9 +267,10 @@ snap_status snap_selftest_bounded_wait(snap_cache* cache, void* stream);
  *  - Limit: the partial results of one call (n * n_q_heads * splits * (d_v + 2) floats,
  *    splits chosen as in snap_decode_attn) must fit SNAP_NOALLOC_SCRATCH_BYTES; larger
  *    batches are rejected with SNAP_ERR_SHAPE (and a line on stderr) before anything is
- *    launched.  Examples that fit: 16 sequences of 32 x 128 GQA heads; 64 sequences of
- *    the same shape with a 8192-slot cache; up to 6 sequences of the 128-head MLA shape
- *    with a 32768-slot cache.
+ *    launched.  Whether a batch fits depends on its split count (snap_decode_attn_plan):
+ *    a call with one split needs no scratch at all (16 sequences of 32 x 128 GQA heads
+ *    with a 32768-slot cache); 64 such sequences with a 8192-slot cache fit; 8 sequences
+ *    of the 128-head MLA shape with a 32768-slot cache fit, 13 do not.
  *  - Set-up: the first call on each device looks up the scratch array's device address
  *    (a host-side query, no allocation) with that device current.  Make that first call
  *    before capturing a stream into a graph.
