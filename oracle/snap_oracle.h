@@ -22,6 +22,11 @@
  * Arithmetic: every input is a bf16 bit pattern (uint16_t); all arithmetic is
  * IEEE double.  Readings of points the pages leave open are listed beside each
  * function.  Parity pins live in tests/test_oracle_pins.py.
+ *
+ * Parity unpinned: which keys the softmax denominator of a window row runs over
+ * (reading: the whole causal row, window included).  No page prints a score, so no
+ * pin fixes that choice; the arithmetic given the reading is pinned (closed forms,
+ * brute force, a textbook softmax row, column mass G*W).
  */
 #ifndef SNAP_ORACLE_H
 #define SNAP_ORACLE_H
@@ -72,7 +77,7 @@ int snap_oracle_plan(const snap_oracle_config* c, int64_t S, snap_oracle_meta* m
  *         at absolute position S-W+w.
  *   lse:  out, [H_kv][W][G]  log-sum-exp of the causal row (reading: the softmax
  *         denominator runs over every key up to and including the query's own
- *         position, window included).
+ *         position, window included; parity unpinned for this reading).
  *   col:  out, [H_kv][S]     sum over (w, g) of the row probability at column j,
  *         for all j < S (window columns included, so each head sums to G*W).
  */
