@@ -838,7 +838,7 @@ def _fill(cache, pool, B, stream):
 
 
 def run_capacity(args):
-    """SURVEY f4 (pages: "Max Batch Size Unlocked"): at a fixed HBM budget for the
+    """Capacity (the pages' "Max Batch Size Unlocked"): at a fixed HBM budget for the
     cache, the largest batch of the workload's prompt length for the fixed-size cache
     and for full KV, and the decode tok/s measured at that batch.  Sequences are filled
     from a pool of 4 seeded prompts (the decode cost depends on the cache, not on which
@@ -879,7 +879,7 @@ def run_capacity(args):
 
 
 def run_sweep(args):
-    """decode tok/s of a batch of 16 GQA (Llama-3.1-8B shape) sequences
+    """Speed sweep: decode tok/s of a batch of 16 GQA (Llama-3.1-8B shape) sequences
     (a) over context length with the cache at a quarter of the prompt (4 sinks, half
     recent) against full KV (the pages' "Throughput by Context Length"), and (b) over the
     cache composition (L_sink, K, L_recent) at 128k, K = 0 being StreamingLLM alone (the
