@@ -435,8 +435,10 @@ def run_ours(args):
     for S in lengths:
         M = (max(wl.L_sink, S - wl.L_recent) if S > wl.L_sink else S) - min(S, wl.L_sink)
         per_step_launches += n_seq_launch if (M > wl.K and wl.K > 0) else 1
-    # decode launches per step: append, attention, split merge
-    per_step_launches += D * 3
+    # decode launches per step: append, attention, and the split merge when the plan
+    # has more than one split (one split at 16 x 128k GQA: no merge kernel runs)
+    splits = cache.decode_attn_plan(B)[0]
+    per_step_launches += D * (3 if splits > 1 else 2)
     traffic = traffic_record(wl.name)
     line = {
         "metric": METRIC,
@@ -457,7 +459,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}",
                    "l2": ("inputs larger than L2 (no flush)" if flush is None
                           else f"L2 flushed before each step ({2 * L2_BYTES >> 20} MiB write)"),
-                   "decode_launch": "cuda graph" if graph is not None else "eager"},
+                   "decode_launch": "cuda graph" if graph is not None else "eager",
+                   "decode_splits": splits},
         "decode_tok_s": B * D * world / (dec_ms / 1e3),
         "decode_ms_per_token_step": dec_ms / D,
         "compress_ms_per_batch": cmp_ms,
