@@ -90,12 +90,14 @@ template <int MODE, bool XRES>
 __device__ __forceinline__ Unit decode_unit(int u, const ScoreParams& p) {
     Unit U;
     if (MODE != COLSUM) {
-        // (h, x tile, split) over row tiles; Y = key tiles up to the tile's causal limit
+        // (h, split, x tile) over row tiles; Y = key tiles up to the tile's causal limit.
+        // The row tiles of one key split are neighbours in u, so the CTAs running at the
+        // same time stream the same key range and share it in L2.
         const int per_h = p.x_tiles * p.splits;
         U.h = u / per_h;
         const int rem = u % per_h;
-        U.xt = rem / p.splits;
-        U.split = rem % p.splits;
+        U.split = rem / p.x_tiles;
+        U.xt = rem % p.x_tiles;
         const int row_last = min(p.R, (U.xt + 1) * XROWS) - 1;
         const int kmax = min(p.S, p.S - p.W + row_last / p.G + 1);
         const int ny = (kmax + p.Ny - 1) / p.Ny;

@@ -180,15 +180,27 @@ ScoreParams score_params(const snap_config& c, int64_t S, const CompressWs& w, u
     return sp;
 }
 
-// Key splits of the row pass: about two units per SM.
+// Key splits of the row pass.  The persistent CTAs take the (head, split, row tile)
+// units in rounds of one per SM, so a split count s costs
+//     ceil(units(s) / SMs) x (key tiles per split + 2)
+// in key-tile times; the 2 covers a unit's start (the resident rows' load and the
+// MMA pipeline's refill).  The smallest cost wins, ties going to fewer splits.
 int row_key_splits(const snap_config& c, int R, int64_t S) {
     const int per = c.n_kv_heads * ((R + 127) / 128);
     const int ny = (int)((S + 255) / 256);
-    int splits = (2 * num_sms() + per - 1) / per;
-    if (splits > MAX_KEY_SPLITS) splits = MAX_KEY_SPLITS;
-    if (splits > ny) splits = ny;
-    if (splits < 1) splits = 1;
-    return splits;
+    const int sms = num_sms();
+    const int top = ny < MAX_KEY_SPLITS ? ny : MAX_KEY_SPLITS;
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int s = 1; s <= top; ++s) {
+        const int64_t rounds = ((int64_t)per * s + sms - 1) / sms;
+        const int64_t cost = rounds * ((ny + s - 1) / s + 2);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
 }
 
 // Row pass: X = 128 observation rows, Y = 256-key tiles.
