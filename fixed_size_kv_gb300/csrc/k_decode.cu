@@ -309,13 +309,8 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
 }  // namespace
 
 cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gqa_decode_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, G_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = opt_in_smem(gqa_decode_kernel, G_SMEM, smem_set); e != cudaSuccess) return e;
     dim3 grid(a.splits, a.cfg.Hkv, a.n);
     return launch_dependent(gqa_decode_kernel, grid, dim3(G_WARPS * 32), G_SMEM, st, a);
 }

@@ -448,28 +448,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 }  // namespace
 
+static std::atomic<uint64_t> mla_smem_set{0};
+
 int mla_decode_wave_ctas() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];     // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-    if (cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
-        return 0;
+    const bool cacheable = dev >= 0 && dev < 64;
+    if (cacheable) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    if (opt_in_smem(mla_decode_tc_kernel, SMEM, mla_smem_set) != cudaSuccess) return 0;
     int per_sm = 0, sms = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mla_decode_tc_kernel, THREADS, SMEM) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || per_sm <= 0)
         return 0;
-    if (dev >= 0 && dev < 64) cached[dev] = per_sm * sms;
+    if (cacheable) cached[dev].store(per_sm * sms, std::memory_order_relaxed);
     return per_sm * sms;
 }
 
 cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    if (cudaError_t e = opt_in_smem(mla_decode_tc_kernel, SMEM, mla_smem_set); e != cudaSuccess) return e;
     dim3 grid(2 * a.splits, a.n);
     return launch_dependent(mla_decode_tc_kernel, grid, dim3(THREADS), SMEM, st, tkv, a);
 }

@@ -384,13 +384,9 @@ template <int MODE, int D, bool XQ, bool XRES>
 cudaError_t launch_inst(const CUtensorMap& tx, const CUtensorMap& ty, const ScoreParams& p, int num_sms,
                         cudaStream_t st) {
     using L = Layout<D, XRES>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(score_tc_kernel<MODE, D, XQ, XRES>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    if (cudaError_t e = opt_in_smem(score_tc_kernel<MODE, D, XQ, XRES>, L::TOTAL, smem_set); e != cudaSuccess)
+        return e;
     const int grid = p.n_units < num_sms ? p.n_units : num_sms;
     if (grid <= 0) return cudaSuccess;
     score_tc_kernel<MODE, D, XQ, XRES><<<grid, THREADS, L::TOTAL, st>>>(tx, ty, p);

@@ -3,6 +3,9 @@
 
 #include <cuda.h>
 
+#include <atomic>
+#include <cstdint>
+
 #include "common.cuh"
 
 namespace snap {
@@ -46,6 +49,21 @@ cudaError_t launch_dependent(void (*kernel)(Exp...), dim3 grid, dim3 block, size
     cfg.attrs = at;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+}
+
+// Opts `kernel` into `bytes` of dynamic shared memory on the current device.  The
+// attribute is per device, so `done` keeps one bit per device (devices 0..63; others
+// set it on every call); concurrent first calls may both set it, which is harmless.
+template <typename... Exp>
+cudaError_t opt_in_smem(void (*kernel)(Exp...), int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
 }
 
 cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);

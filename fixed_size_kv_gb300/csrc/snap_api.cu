@@ -34,17 +34,21 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// SMs of the current device (cached per device).  If the query fails, 1: the plans
+// built from it stay valid (the persistent kernels loop over their units), and the
+// failure itself surfaces at the next launch.
 int num_sms() {
-    static int cached = 0;
-    if (cached == 0) {
-        int dev = 0, n = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess &&
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-            cached = n;
-        else
-            return 148;
+    static std::atomic<int> cached[64];     // zero-initialised (static storage)
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const bool cacheable = dev >= 0 && dev < 64;
+    if (cacheable) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
     }
-    return cached;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+    if (cacheable) cached[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 DevConfig dev_config(const snap_config& c, int max_batch) {
