@@ -86,6 +86,8 @@ def _load():
             lib.snap_oracle_select.restype = i64
             lib.snap_oracle_compress.argtypes = [P(_Config), i64, vp, vp, i64, i64, vp, vp, vp,
                                                  vp, vp, P(_Meta)]
+            lib.snap_oracle_compress_scored.argtypes = [P(_Config), i64, vp, vp, i64, i64, vp, vp, vp,
+                                                        vp, vp, P(_Meta)]
             lib.snap_oracle_ring_slot.argtypes = [P(_Config), i64]
             lib.snap_oracle_ring_slot.restype = i64
             lib.snap_oracle_slot_valid.argtypes = [P(_Config), P(_Meta), i64]
@@ -183,6 +185,36 @@ def window_scores(cfg: Config, K, Q):
     return lse, col
 
 
+def window_columns(cfg: Config, K, Q, threads: int = 1, group: int = 0) -> np.ndarray:
+    """The column scores of window_scores(cfg, K, Q) ([H_kv][S]), computed as sums over
+    groups of `group` query heads (default: one group per KV head) with one
+    window_scores call per (KV head, group), run on `threads` threads (the C oracle
+    releases the GIL).  The scores are sums over observation rows, so the grouping
+    changes only the order of the double-precision additions."""
+    from concurrent.futures import ThreadPoolExecutor
+    import torch
+    G = cfg.G
+    group = G if group <= 0 else group
+    assert G % group == 0, (G, group)
+    Kt = K if hasattr(K, "detach") else torch.from_numpy(np.ascontiguousarray(K)).view(torch.bfloat16)
+    Qt = Q if hasattr(Q, "detach") else torch.from_numpy(np.ascontiguousarray(Q)).view(torch.bfloat16)
+    S = Kt.shape[0]
+    sub = Config(cfg.layout, group, 1, cfg.d_qk, cfg.d_v, cfg.L_sink, cfg.K, cfg.L_recent, cfg.W, cfg.P,
+                 cfg.sm_scale)
+    jobs = [(h, g0) for h in range(cfg.n_kv_heads) for g0 in range(0, G, group)]
+
+    def run(job):
+        h, g0 = job
+        q0 = h * G + g0
+        return window_scores(sub, Kt[:, h:h + 1].contiguous(), Qt[:, q0:q0 + group].contiguous())[1][0]
+
+    col = np.zeros((cfg.n_kv_heads, S), np.float64)
+    with ThreadPoolExecutor(max(1, threads)) as ex:
+        for (h, _), c in zip(jobs, ex.map(run, jobs)):
+            col[h] += c
+    return col
+
+
 def maxpool(x, P: int) -> np.ndarray:
     x = np.ascontiguousarray(x, np.float64)
     y = np.zeros_like(x)
@@ -224,9 +256,12 @@ class Cache:
         return out
 
 
-def compress(cfg: Config, K, V, Q, want_pool: bool = False) -> Cache:
-    """K/V: [S][H_kv][d] bf16 (V None for MLA); Q: [W][H_q][d_qk] bf16."""
-    kb, qb = _bits(K), _bits(Q)
+def compress(cfg: Config, K, V, Q, want_pool: bool = False, col=None) -> Cache:
+    """K/V: [S][H_kv][d] bf16 (V None for MLA); Q: [W][H_q][d_qk] bf16.  With `col`
+    ([H_kv][S] column scores, e.g. from window_columns) the scoring step is taken from
+    it instead of being recomputed from Q (Q may then be None)."""
+    kb = _bits(K)
+    qb = _bits(Q) if Q is not None else None
     vb = _bits(V) if V is not None else None
     S = kb.shape[0]
     C, H = cfg.C, cfg.n_kv_heads
@@ -235,10 +270,18 @@ def compress(cfg: Config, K, V, Q, want_pool: bool = False) -> Cache:
     sel = np.full((H, max(cfg.K, 1)), -1, np.int32)
     pool = np.zeros((H, max(S - cfg.W, 1)), np.float64) if want_pool else None
     m = _Meta()
-    rc = _load().snap_oracle_compress(
-        ctypes.byref(cfg._c()), S, _ptr(kb), _ptr(vb) if vb is not None else None,
-        H * cfg.d_qk, cfg.d_qk, _ptr(qb), _ptr(ck), _ptr(cv) if cv is not None else None,
-        _ptr(sel), _ptr(pool) if pool is not None else None, ctypes.byref(m))
+    if col is not None:
+        colb = np.ascontiguousarray(col, np.float64)
+        assert colb.shape == (H, S), colb.shape
+        rc = _load().snap_oracle_compress_scored(
+            ctypes.byref(cfg._c()), S, _ptr(kb), _ptr(vb) if vb is not None else None,
+            H * cfg.d_qk, cfg.d_qk, _ptr(colb), _ptr(ck), _ptr(cv) if cv is not None else None,
+            _ptr(sel), _ptr(pool) if pool is not None else None, ctypes.byref(m))
+    else:
+        rc = _load().snap_oracle_compress(
+            ctypes.byref(cfg._c()), S, _ptr(kb), _ptr(vb) if vb is not None else None,
+            H * cfg.d_qk, cfg.d_qk, _ptr(qb), _ptr(ck), _ptr(cv) if cv is not None else None,
+            _ptr(sel), _ptr(pool) if pool is not None else None, ctypes.byref(m))
     if rc != 0:
         raise ValueError(f"oracle compress rc={rc}")
     return Cache(cfg, ck, cv, sel[:, :cfg.K], Meta._from(m), pool)

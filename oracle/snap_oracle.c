@@ -184,10 +184,12 @@ static void copy_row(uint16_t* dst, const uint16_t* src, int n)
     memcpy(dst, src, sizeof(uint16_t) * (size_t)n);
 }
 
-int snap_oracle_compress(const snap_oracle_config* c, int64_t S,
+/* Compression; the column scores come from window_scores(Q) when col_in is NULL,
+ * else from col_in ([H_kv][S], the same quantity computed by the caller). */
+static int compress_core(const snap_oracle_config* c, int64_t S,
                          const uint16_t* Kp, const uint16_t* Vp,
                          int64_t k_tok_stride, int64_t k_head_stride,
-                         const uint16_t* Q,
+                         const uint16_t* Q, const double* col_in,
                          uint16_t* cache_k, uint16_t* cache_v,
                          int32_t* sel, double* pool, snap_oracle_meta* m)
 {
@@ -209,8 +211,13 @@ int snap_oracle_compress(const snap_oracle_config* c, int64_t S,
         double* col = (double*)malloc(sizeof(double) * (size_t)(Hkv * S));
         double* pl = (double*)malloc(sizeof(double) * (size_t)n_scored);
         if (!lse || !col || !pl) { free(lse); free(col); free(pl); return -3; }
-        int rc = snap_oracle_window_scores(c, S, Kp, k_tok_stride, k_head_stride, Q, lse, col);
-        if (rc != 0) { free(lse); free(col); free(pl); return rc; }
+        if (col_in) {
+            memcpy(col, col_in, sizeof(double) * (size_t)(Hkv * S));
+        } else {
+            if (!Q) { free(lse); free(col); free(pl); return -1; }
+            int rc = snap_oracle_window_scores(c, S, Kp, k_tok_stride, k_head_stride, Q, lse, col);
+            if (rc != 0) { free(lse); free(col); free(pl); return rc; }
+        }
         for (int h = 0; h < Hkv; ++h) {
             /* pool over the scored prefix [0, S-W), then select in the middle */
             snap_oracle_maxpool(col + (int64_t)h * S, n_scored, c->P, pl);
@@ -244,6 +251,29 @@ int snap_oracle_compress(const snap_oracle_config* c, int64_t S,
         }
     }
     return 0;
+}
+
+int snap_oracle_compress(const snap_oracle_config* c, int64_t S,
+                         const uint16_t* Kp, const uint16_t* Vp,
+                         int64_t k_tok_stride, int64_t k_head_stride,
+                         const uint16_t* Q,
+                         uint16_t* cache_k, uint16_t* cache_v,
+                         int32_t* sel, double* pool, snap_oracle_meta* m)
+{
+    return compress_core(c, S, Kp, Vp, k_tok_stride, k_head_stride, Q, NULL, cache_k, cache_v, sel,
+                         pool, m);
+}
+
+int snap_oracle_compress_scored(const snap_oracle_config* c, int64_t S,
+                                const uint16_t* Kp, const uint16_t* Vp,
+                                int64_t k_tok_stride, int64_t k_head_stride,
+                                const double* col,
+                                uint16_t* cache_k, uint16_t* cache_v,
+                                int32_t* sel, double* pool, snap_oracle_meta* m)
+{
+    if (!col) return -1;
+    return compress_core(c, S, Kp, Vp, k_tok_stride, k_head_stride, NULL, col, cache_k, cache_v, sel,
+                         pool, m);
 }
 
 /* Number of ring-held positions and the oldest one, at length T. */

@@ -110,6 +110,20 @@ int snap_oracle_compress(const snap_oracle_config* c, int64_t S,
                          uint16_t* cache_k, uint16_t* cache_v,
                          int32_t* sel, double* pool, snap_oracle_meta* m);
 
+/*
+ * snap_oracle_compress() with the column scores supplied instead of the window
+ * queries: col [H_kv][S] is what snap_oracle_window_scores() returns in `col`.  The
+ * scores are additive over the observation rows, so a caller may compute them as
+ * sums over disjoint groups of query heads (one window_scores call per group).
+ * Everything after scoring (pool, select, cache layout) is snap_oracle_compress().
+ */
+int snap_oracle_compress_scored(const snap_oracle_config* c, int64_t S,
+                                const uint16_t* Kp, const uint16_t* Vp,
+                                int64_t k_tok_stride, int64_t k_head_stride,
+                                const double* col,
+                                uint16_t* cache_k, uint16_t* cache_v,
+                                int32_t* sel, double* pool, snap_oracle_meta* m);
+
 /* Ring slot (within the whole cache) that holds absolute position p. */
 int64_t snap_oracle_ring_slot(const snap_oracle_config* c, int64_t p);
 

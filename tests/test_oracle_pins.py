@@ -228,6 +228,38 @@ def test_compress_selection_matches_scores(oracle_lib):
         assert cache.sel[h].tolist() == expect.tolist()
 
 
+def test_compress_from_supplied_scores_is_the_same_compression(oracle_lib):
+    """Compression with the column scores supplied (the path the large parity tests use
+    to score on several threads) is bit-identical to compression from the queries."""
+    c = cfg_of(Hq=8, Hkv=2, dk=16, L_sink=3, K=7, L_recent=8, W=4, P=5)
+    S = 80
+    K, V, Q = bf16((S, 2, 16), 21), bf16((S, 2, 16), 22), bf16((4, 8, 16), 23)
+    ref = oracle.compress(c, K, V, Q, want_pool=True)
+    _, col = oracle.window_scores(c, K, Q)
+    got = oracle.compress(c, K, V, None, want_pool=True, col=col)
+    np.testing.assert_array_equal(got.sel, ref.sel)
+    np.testing.assert_array_equal(got.k, ref.k)
+    np.testing.assert_array_equal(got.v, ref.v)
+    np.testing.assert_array_equal(got.pool, ref.pool)
+    assert got.meta == ref.meta
+
+
+@pytest.mark.parametrize("layout,Hq,Hkv,group", [(0, 8, 2, 2), (0, 8, 2, 0), (1, 16, 1, 4)])
+def test_window_columns_by_head_groups(oracle_lib, layout, Hq, Hkv, group):
+    """Column scores summed over disjoint groups of query heads, scored on several
+    threads, equal the one-call scores up to the order of the double additions; the
+    MLA case checks the per-head mass as well (each query head's W rows sum to W)."""
+    dk = 24 if layout == 1 else 16
+    dv = 16
+    c = cfg_of(layout=layout, Hq=Hq, Hkv=Hkv, dk=dk, dv=dv, L_sink=2, K=5, L_recent=8, W=4, P=3)
+    S = 50
+    K, Q = bf16((S, Hkv, dk), 31), bf16((4, Hq, dk), 32)
+    _, col = oracle.window_scores(c, K, Q)
+    got = oracle.window_columns(c, K, Q, threads=3, group=group)
+    np.testing.assert_allclose(got, col, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(got.sum(axis=1), np.full(Hkv, c.G * c.W), rtol=1e-12)
+
+
 def test_cache_is_four_times_smaller(oracle_lib):
     """The page's 4.0x lower KV memory at 128K context with a 32k cache."""
     with open(os.path.join(GOLDEN, "pages_figures.json")) as f:
