@@ -729,6 +729,11 @@ extern "C" snap_status snap_decode_attn_noalloc(snap_cache* cache, const int32_t
     a.out = static_cast<float*>(out);
     a.status = cache->status;
     a.cfg = dev_config(c, cache->max_batch);
+    // The scratch address is looked up on every device's first call, whatever its
+    // split plan, so that this first call (which may also load the module holding
+    // the array) is the one the header tells callers to make before any capture.
+    void* scratch = nullptr;
+    if (const snap_status s = noalloc_scratch(&scratch); s != SNAP_OK) return s;
     int splits = 1;
     decode_plan(cache, n, &splits, &a.tiles_per_split);
     a.splits = splits;
@@ -744,9 +749,6 @@ extern "C" snap_status snap_decode_attn_noalloc(snap_cache* cache, const int32_t
                          need, n, SNAP_NOALLOC_SCRATCH_BYTES);
             return SNAP_ERR_SHAPE;
         }
-        void* scratch = nullptr;
-        const snap_status s = noalloc_scratch(&scratch);
-        if (s != SNAP_OK) return s;
         a.part_o = static_cast<float*>(scratch);
         a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + o_bytes);
     }

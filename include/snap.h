@@ -256,9 +256,9 @@ snap_status snap_selftest_bounded_wait(snap_cache* cache, void* stream);
  * no counterpart: this is a packaging variant of the same decode attention.
  *
  * Who needs it: code that runs where cudaMalloc is unavailable or unwelcome, for
- * example inside a host callback, a signal-safe or real-time thread, a stream
- * being captured into a CUDA graph, or an embedding runtime that owns every device
- * allocation itself.  Such a caller cannot obtain the workspace snap_decode_attn()
+ * example a real-time thread that must not block in the allocator, a stream being
+ * captured into a CUDA graph (after this entry point's first call on the device), or
+ * an embedding runtime that owns every device allocation itself.  Such a caller cannot obtain the workspace snap_decode_attn()
  * needs for its split-KV partial results.  This entry point takes the same inputs
  * and output (q, out, slots; the cache it attends over) and keeps the partial results
  * in a fixed scratch array compiled into the library instead.  It never calls
@@ -271,9 +271,11 @@ snap_status snap_selftest_bounded_wait(snap_cache* cache, void* stream);
  *    a call with one split needs no scratch at all (16 sequences of 32 x 128 GQA heads
  *    with a 32768-slot cache); 64 such sequences with a 8192-slot cache fit; 8 sequences
  *    of the 128-head MLA shape with a 32768-slot cache fit, 13 do not.
- *  - Set-up: the first call on each device looks up the scratch array's device address
- *    (a host-side query, no allocation) with that device current.  Make that first call
- *    before capturing a stream into a graph.
+ *  - Set-up: the first call on each device, whatever its batch, looks up the scratch
+ *    array's device address (cudaGetSymbolAddress, with that device current).  That
+ *    lookup may also load the library module holding the array, which is when the
+ *    32 MiB are reserved on the device.  Make that first call before capturing a
+ *    stream into a graph.
  *  - Sharing: every call on a device uses the same array, and it keeps the previous
  *    call's contents.  Each call overwrites every partial it reads, so nothing needs
  *    clearing, but calls that overlap on the GPU (different streams without ordering,

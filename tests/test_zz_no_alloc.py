@@ -1,8 +1,8 @@
 """snap_decode_attn_noalloc: decode attention for callers that cannot allocate.
 
-Some callers (a host callback, a real-time thread, a stream under graph capture,
-a runtime that owns every allocation) cannot provide the device workspace that
-snap_decode_attn needs for its split-KV partial results.  The no-alloc entry point
+Some callers (a real-time thread that must not block in the allocator, a stream
+under graph capture, a runtime that owns every device allocation) cannot provide the
+device workspace that snap_decode_attn needs for its split-KV partial results.  The no-alloc entry point
 keeps those partials in a fixed scratch array inside the library.  These tests call
 it through the C ABI and check it against the workspace entry point on the same
 cache, on two calls in a row (the scratch keeps the previous call's contents, which
@@ -18,9 +18,6 @@ import torch
 from fixed_size_kv_gb300 import inputs, snap
 
 pytestmark = pytest.mark.gpu
-
-MAX_ABS, MEAN_ABS = 2e-2, 5e-3
-
 
 def _cfg(wl):
     return snap.make_config(**wl.config_kwargs())
@@ -56,9 +53,9 @@ def test_noalloc_matches_workspace_entry_point_twice(layout):
         assert status == snap.SNAP_OK, snap.status_string(status)
         torch.cuda.synchronize()
         assert cache.check_device() == snap.SNAP_OK
-        d = (out - ref).abs()
         assert bool(torch.isfinite(out).all())
-        assert d.max().item() <= MAX_ABS and d.mean().item() <= MEAN_ABS, (step, d.max().item())
+        # the same kernels with the same split plan: a stale partial would show as a difference
+        assert torch.equal(out, ref), (step, (out - ref).abs().max().item())
 
 
 def _scratch_need(n, heads, splits, d_v):
