@@ -63,17 +63,6 @@ def gpu_meta(cache: snap.SnapCache, slot: int) -> dict:
     return dict(S=m[0], T=m[1], R0=m[2], n_sink=m[3], n_mid=m[4])
 
 
-def oracle_cache_from_gpu(cache: snap.SnapCache, slot: int, ocfg: oracle.Config) -> oracle.Cache:
-    """The GPU's cache of one sequence as an oracle cache (to check decode in isolation)."""
-    m = gpu_meta(cache, slot)
-    k = bits(cache.k_cache()[slot])
-    v = bits(cache.v_cache()[slot]) if cache.v_cache() is not None else None
-    sel = cache.selected()[slot].cpu().numpy().astype(np.int32) if ocfg.K > 0 else \
-        np.zeros((ocfg.n_kv_heads, 0), np.int32)
-    meta = oracle.Meta(S=m["S"], T=m["T"], n_sink=m["n_sink"], R0=m["R0"], n_mid=m["n_mid"])
-    return oracle.Cache(ocfg, k, v, sel, meta)
-
-
 def check_cache_rows(cache: snap.SnapCache, slot: int, ocache: oracle.Cache, K_all: torch.Tensor,
                      V_all: torch.Tensor | None, where: str = "") -> None:
     """Every valid slot of the GPU cache holds, bit-exactly, the row of the position the
@@ -103,3 +92,31 @@ def check_cache_rows(cache: snap.SnapCache, slot: int, ocache: oracle.Cache, K_a
                 raise AssertionError(f"{where}: K row mismatch head {h} slot {s} position {p}")
             if vb is not None and not np.array_equal(gv[h, s], vb[p, h]):
                 raise AssertionError(f"{where}: V row mismatch head {h} slot {s} position {p}")
+
+
+def one_head_workload(wl: inputs.Workload) -> inputs.Workload:
+    """The problem of one KV head alone: that head and its G query heads (every step of
+    the method is independent across KV heads)."""
+    return wl.replace(n_q_heads=wl.G, n_kv_heads=1)
+
+
+def oracle_head_cache(wl: inputs.Workload, K: torch.Tensor, V: torch.Tensor | None, Q: torch.Tensor, h: int,
+                      threads: int = 1, group: int = 0) -> oracle.Cache:
+    """The oracle's cache of KV head h of one sequence, built from the prompt alone:
+    K/V [S][H_kv][d] and Q [W][H_q][d] (CPU bf16).  Scoring runs on `threads` threads over
+    groups of `group` query heads (oracle.window_columns).  pool holds the pooled scores."""
+    G = wl.G
+    one = one_head_workload(wl)
+    ocfg = oracle_cfg(one)
+    K1 = K[:, h:h + 1].contiguous()
+    V1 = V[:, h:h + 1].contiguous() if V is not None else None
+    Q1 = Q[:, h * G:(h + 1) * G].contiguous()
+    m = oracle.plan(ocfg, K1.shape[0])
+    scored = wl.K > 0 and m.R0 - m.n_sink > wl.K
+    col = oracle.window_columns(ocfg, K1, Q1, threads=threads, group=group) if scored else None
+    return oracle.compress(ocfg, K1, V1, Q1, want_pool=True, col=col)
+
+
+def oracle_workers() -> int:
+    import os
+    return max(1, os.cpu_count() or 1)

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from fixed_size_kv_gb300 import inputs, snap
-from parity import (check_cache_rows, check_outputs, oracle_cache_from_gpu, oracle_cfg, snap_cfg)
+from parity import check_cache_rows, check_outputs, oracle_cfg, snap_cfg
 
 pytestmark = pytest.mark.gpu
 
@@ -39,7 +39,7 @@ class Batch:
         self.dslots = torch.tensor(self.slots, dtype=torch.int32, device="cuda")
         self.seed = seed
 
-    def step(self, t, append=True, isolated=False, fused=False):
+    def step(self, t, append=True, fused=False):
         wl, n = self.wl, len(self.slots)
         tok = inputs.gen_decode(wl, n, step=t, seed=self.seed)
         if fused:
@@ -57,10 +57,7 @@ class Batch:
                 self.K[i] = torch.cat([self.K[i], tok.k[i:i + 1]])
                 if tok.v is not None:
                     self.V[i] = torch.cat([self.V[i], tok.v[i:i + 1]])
-            oc = self.ocaches[i]
-            if isolated:  # the oracle reads the GPU's own cache
-                oc = oracle_cache_from_gpu(self.cache, self.slots[i], oracle_cfg(wl))
-            check_outputs(out[i], oracle.decode_attn(oc, tok.q[i]), f"step {t} seq {i}")
+            check_outputs(out[i], oracle.decode_attn(self.ocaches[i], tok.q[i]), f"step {t} seq {i}")
         return out
 
     def check_rows(self):
@@ -85,18 +82,18 @@ def test_decode_continuous_batch_ring_offsets():
     lengths = [300, 37, 129, 2, 1000]
     b = Batch(wl, lengths, slots=[3, 0, 6, 1, 4], seed=9, max_batch=8)
     for t in range(80):
-        b.step(t, isolated=(t % 20 == 0))
+        b.step(t)
     b.check_rows()
 
 
 def test_fused_decode_step_continuous_batch():
-    """snap_decode_step (append + attention in one launch) over a continuous batch at
+    """snap_decode_step (append, then attention, on one stream) over a continuous batch at
     different ring offsets, with splits (cache 4096) and without (cache 128)."""
     for C_parts, lengths in (((4, 2044, 2048), [6000, 300, 2100, 4500]), ((4, 60, 64), [300, 37, 129, 2])):
         wl = inputs.Workload("fused", 0, 32, 8, 128, 128, *C_parts, 16, 7, 4, 0, 0, 0, 1 / math.sqrt(128))
         b = Batch(wl, lengths, slots=[2, 0, 3, 1], seed=17, max_batch=4)
         for t in range(70):
-            b.step(t, fused=True, isolated=(t == 69))
+            b.step(t, fused=True)
         b.check_rows()
 
 
@@ -156,7 +153,7 @@ def test_decode_mla_small():
                          1 / math.sqrt(192))
     b = Batch(wl, [700, 90], [1, 0], seed=12)
     for t in range(110):
-        b.step(t, isolated=(t == 109))
+        b.step(t)
     b.check_rows()
 
 
@@ -166,7 +163,7 @@ def test_decode_mla_long_cache_splits():
                          1 / math.sqrt(192))
     b = Batch(wl, [6000, 2500, 4100], [0, 1, 2], seed=13)
     for t in range(3):
-        b.step(t, isolated=(t == 2))
+        b.step(t)
 
 
 def test_decode_out_of_range_slot_reports_without_fault():
