@@ -54,6 +54,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-full-kv", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the short runs of the other four workloads that the 128k line carries")
     p.add_argument("--capacity", type=float, default=0.0, metavar="GIB",
                    help="extra mode: the largest batch whose cache fits GIB of HBM, fixed-size cache vs full "
                         "KV, with decode tok/s measured at that batch (one JSON line per cache kind)")
@@ -200,28 +202,56 @@ def algorithmic_decode_bytes(wl, metas):
     return valid * row + n * wl.n_q_heads * (wl.d_qk * 2 + wl.d_v * 4)
 
 
-def run_ours(args):
+def workload_config(wl, B, lengths, world):
+    """The workload description both arms print (the GPU arm and the oracle arm)."""
+    return {"workload": wl.name, "batch": B, "prompt_len": max(lengths), "decode_steps": wl.decode_steps,
+            "cache": f"{wl.L_sink}+{wl.K}+{wl.L_recent}={wl.C}", "W": wl.W, "P": wl.P,
+            "heads": f"{wl.n_q_heads}/{wl.n_kv_heads}x{wl.d_qk}", "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+def score_pass_flop(wl, lengths):
+    """Algorithmic FLOP of one score GEMM pass per sequence (mean over the batch):
+    2 R d S per KV head, R = G W observation rows (the compression's one dense contraction)."""
+    return statistics.mean(2.0 * wl.G * wl.W * wl.d_qk * S * wl.n_kv_heads for S in lengths)
+
+
+def time_compress_stages(cache, pre, stream, lses=None, reps=2):
+    """Per-sequence CUDA-event times (ms) of each compression stage, each stage launched
+    on its own between events (snap_compress_stages); the last of `reps` passes."""
     import torch
-    import torch.distributed as dist
+    from fixed_size_kv_gb300 import snap
+    stages = [("rows", snap.STAGE_ROWS), ("columns", snap.STAGE_COLUMNS), ("select", snap.STAGE_SELECT),
+              ("write", snap.STAGE_WRITE)]
+    B = len(pre)
+    out = {}
+    for _ in range(reps):
+        evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in stages]
+               for _ in range(B)]
+        for b in range(B):
+            p = pre[b]
+            for i, (_, bit) in enumerate(stages):
+                evs[b][i][0].record(stream)
+                cache.compress_stages(b, p.K, p.V, p.Q, bit, lse_obs=None if lses is None else lses[b],
+                                      stream=stream)
+                evs[b][i][1].record(stream)
+        stream.synchronize()
+        out = {name: statistics.mean(evs[b][i][0].elapsed_time(evs[b][i][1]) for b in range(B))
+               for i, (name, _) in enumerate(stages)}
+    return out
 
-    from fixed_size_kv_gb300 import inputs, snap
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    snap.load(build_if_missing=True)
+def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
+    """One workload on this GPU: `warmup` untimed steps, then `steps` timed steps of
+    (compress every prompt, then every decode step of the batch, the decode loop
+    replayed as one CUDA graph unless --eager).  Returns the JSON fields of the
+    workload (without the CPU baseline and the end-to-end run)."""
+    import torch
 
-    wl = inputs.WORKLOADS[args.workload]
-    if args.batch:
-        wl = wl.replace(batch=args.batch)
+    from fixed_size_kv_gb300 import snap
+
     B, D = wl.batch, wl.decode_steps
-    stream = torch.cuda.Stream(device=dev)
     hbm_peak, bf16_sus, bf16_burst, peak_kind = peaks()
-
     with torch.cuda.stream(stream):
         lengths, pre, q_all, k_all, v_all = make_batch(wl, args.seed, rank, dev)
     stream.synchronize()
@@ -229,11 +259,11 @@ def run_ours(args):
     cache = snap.SnapCache(cfg, max_batch=B, max_prompt=max(lengths), max_n=B, device=dev, stream=stream)
     slots = torch.arange(B, dtype=torch.int32, device=dev)
     out = torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev)
-    split_count = None
 
     def barrier():
         torch.cuda.synchronize(dev)
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
 
     def one_step(c, prefill, record=None):
@@ -261,7 +291,7 @@ def run_ours(args):
         return {"s0": E(), "c0": E(), "c1": E(), "d1": E(),
                 "a0": [E() for _ in range(D)], "a1": [E() for _ in range(D)]}
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         one_step(cache, pre)
     barrier()
     graph = None
@@ -278,7 +308,7 @@ def run_ours(args):
         stream.synchronize()
     st = cache.check_device(stream)
     if st != snap.SNAP_OK:
-        raise RuntimeError(f"device status after warm-up: {snap.status_string(st)}")
+        raise RuntimeError(f"{wl.name}: device status after warm-up: {snap.status_string(st)}")
     metas = [tuple(r[:5]) for r in cache.meta().cpu().tolist()]
     # the decode launches see T = S .. S + D - 1; bytes at the middle step stand for all
     mid_metas = [(S, S + D // 2, R0, ns, nm) for (S, T, R0, ns, nm) in
@@ -291,12 +321,13 @@ def run_ours(args):
     flush = None
     if work_bytes < 4 * L2_BYTES:
         flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-    clocks = ClockSampler(local)
-    clocks.start()
-    evs = [new_events() for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index or 0) if full_run else None
+    if clocks:
+        clocks.start()
+    evs = [new_events() for _ in range(steps)]
     barrier()
     t_wall = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         if flush is not None:  # evict the previous step's data from L2 (not timed)
             with torch.cuda.stream(stream):
                 flush.fill_(i & 255)
@@ -313,10 +344,10 @@ def run_ours(args):
             evs[i]["d1"].record(stream)
     barrier()
     t_wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
-    step_ms = [evs[i]["s0"].elapsed_time(evs[i]["d1"]) for i in range(args.steps)]
-    compress_ms = [evs[i]["c0"].elapsed_time(evs[i]["c1"]) for i in range(args.steps)]
-    decode_ms = [evs[i]["c1"].elapsed_time(evs[i]["d1"]) for i in range(args.steps)]
+    clk = clocks.stop() if clocks else None
+    step_ms = [evs[i]["s0"].elapsed_time(evs[i]["d1"]) for i in range(steps)]
+    compress_ms = [evs[i]["c0"].elapsed_time(evs[i]["c1"]) for i in range(steps)]
+    decode_ms = [evs[i]["c1"].elapsed_time(evs[i]["d1"]) for i in range(steps)]
     if graph is not None:
         # per-launch attention time from one more pass of the same calls, launched one by one
         ev = new_events()
@@ -324,19 +355,16 @@ def run_ours(args):
         stream.synchronize()
         evs = [ev]
     attn_ms = [sum(e["a0"][t].elapsed_time(e["a1"][t]) for t in range(D)) / D for e in evs]
-    total_ms = sum(step_ms)
     st = cache.check_device(stream)
     if st != snap.SNAP_OK:
-        raise RuntimeError(f"device status after timed steps: {snap.status_string(st)}")
+        raise RuntimeError(f"{wl.name}: device status after timed steps: {snap.status_string(st)}")
 
     def reduce_max(x):
         return max_over_ranks(x, world, dev)
 
-    total_ms = reduce_max(total_ms)
-    ms_step = total_ms / args.steps
-    value = job_throughput(B * D * args.steps, world, total_ms)
-    dec_ms = reduce_max(sum(decode_ms)) / args.steps
-    cmp_ms = reduce_max(sum(compress_ms)) / args.steps
+    total_ms = reduce_max(sum(step_ms))
+    dec_ms = reduce_max(sum(decode_ms)) / steps
+    cmp_ms = reduce_max(sum(compress_ms)) / steps
     attn_avg_ms = statistics.mean(attn_ms)
     attn_gbs = attn_bytes / (attn_avg_ms / 1e3) / 1e9
 
@@ -394,35 +422,153 @@ def run_ours(args):
         f_bytes = algorithmic_decode_bytes(full_wl, fmetas)
         full = {"decode_tok_s": B * D * world / (f_ms / 1e3), "decode_ms_per_token_step": f_ms / D,
                 "attn_ms": f_attn, "attn_hbm_gbs": f_bytes / (f_attn / 1e3) / 1e9,
+                "attn_frac": f_bytes / (f_attn / 1e3) / 1e9 / hbm_peak,
                 "cache_bytes": snap.cache_bytes(fcfg, B)}
         del fcache, fgraph
         torch.cuda.empty_cache()
 
-    # ---------------------------------------------------------------- compression when the prefill
-    # supplies the window rows' log-sum-exp (snap_compress_lse: the row pass is skipped)
-    cmp_lse_ms = None
-    if rank == 0 and not args.no_full_kv:
-        lses = [window_lse(wl, p.K, p.Q) for p in pre]
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for rep in range(2):
-            e0.record(stream)
-            for b in range(B):
-                cache.compress_lse(b, pre[b].K, pre[b].V, pre[b].Q, lses[b], stream=stream)
-            e1.record(stream)
-            stream.synchronize()
-        cmp_lse_ms = e0.elapsed_time(e1) / B
-        del lses
+    # ---------------------------------------------------------------- compression, stage by stage,
+    # and with the prefill's log-sum-exp supplied (snap_compress_lse: no row pass)
+    lses = [window_lse(wl, p.K, p.Q) for p in pre]
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for rep in range(2):
+        e0.record(stream)
+        for b in range(B):
+            cache.compress_lse(b, pre[b].K, pre[b].V, pre[b].Q, lses[b], stream=stream)
+        e1.record(stream)
+        stream.synchronize()
+    cmp_lse_ms = e0.elapsed_time(e1) / B
+    stage_ms = time_compress_stages(cache, pre, stream)
+    del lses
+    F = score_pass_flop(wl, lengths)
+    tf = lambda ms: F / (ms / 1e3) / 1e12 if ms else None  # noqa: E731
+    scored = any((max(wl.L_sink, S - wl.L_recent) if S > wl.L_sink else S) - min(S, wl.L_sink) > wl.K > 0
+                 for S in lengths)
+    compress_roofline = None
+    if scored:
+        compress_roofline = {
+            "bound": "tensor", "unit": "TFLOP/s", "peak": bf16_burst,
+            "peak_kind": "bf16 burst (each pass timed on its own)", "peak_source": peak_kind,
+            "flop_per_pass_per_seq": F,
+            "row_pass": {"ms": stage_ms["rows"], "achieved": tf(stage_ms["rows"]),
+                         "frac": tf(stage_ms["rows"]) / bf16_burst,
+                         "note": "row-statistics GEMM plus the small merge of its per-split partials"},
+            "column_pass": {"ms": stage_ms["columns"], "achieved": tf(stage_ms["columns"]),
+                            "frac": tf(stage_ms["columns"]) / bf16_burst},
+            "select_ms": stage_ms["select"], "cache_write_ms": stage_ms["write"],
+            "whole_call": {"ms": cmp_ms / B, "achieved": tf(cmp_ms / B), "frac": tf(cmp_ms / B) / bf16_burst,
+                           "note": "snap_compress per sequence against one GEMM's FLOP"},
+            "whole_call_with_prefill_lse": {"ms": cmp_lse_ms, "achieved": tf(cmp_lse_ms),
+                                            "frac": tf(cmp_lse_ms) / bf16_burst},
+        }
+    cache_write_bytes = statistics.mean(2 * wl.n_kv_heads * wl.C * (wl.d_qk + (wl.d_v if wl.layout == 0 else 0)) * 2
+                                        for _ in lengths)
+
+    splits = cache.decode_attn_plan(B)[0]
+    n_seq_launch = 5  # rowstat, lse merge, colsum, select, cache write (scored prompts)
+    per_step_launches = 0
+    for S in lengths:
+        M = (max(wl.L_sink, S - wl.L_recent) if S > wl.L_sink else S) - min(S, wl.L_sink)
+        per_step_launches += n_seq_launch if (M > wl.K and wl.K > 0) else 1
+    per_step_launches += D * decode_launches_per_step(splits)
+    res = {
+        "lengths": lengths, "pre": pre, "q_all": q_all, "k_all": k_all, "v_all": v_all, "cfg": cfg,
+        "B": B, "D": D, "steps": steps, "graph": graph is not None, "flush": flush is not None,
+        "splits": splits, "value": job_throughput(B * D * steps, world, total_ms),
+        "ms_per_step": total_ms / steps, "clk": clk, "t_wall": t_wall,
+        "fields": {
+            "decode_tok_s": B * D * world / (dec_ms / 1e3),
+            "decode_ms_per_token_step": dec_ms / D,
+            "compress_ms_per_batch": cmp_ms,
+            "compress_ms_per_seq": cmp_ms / B,
+            "compress_with_prefill_lse_ms_per_seq": cmp_lse_ms,
+            "compress_stage_ms_per_seq": stage_ms,
+            "attn": {"ms": attn_avg_ms, "hbm_gbs": attn_gbs, "bytes_per_launch": attn_bytes,
+                     "frac": attn_gbs / hbm_peak},
+            "full_kv": full,
+            "speedup_vs_full_kv": (B * D * world / (dec_ms / 1e3)) / full["decode_tok_s"] if full else None,
+            "cache_bytes": snap.cache_bytes(cfg, B),
+            "cache_write": {"ms": stage_ms["write"], "bytes_per_seq": cache_write_bytes,
+                            "hbm_gbs": cache_write_bytes / (stage_ms["write"] / 1e3) / 1e9,
+                            "frac": cache_write_bytes / (stage_ms["write"] / 1e3) / 1e9 / hbm_peak},
+            "roofline": {"bound": "hbm", "kernel": decode_kernel_name(wl),
+                         "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": attn_gbs / hbm_peak, "peak_source": peak_kind,
+                         "traffic": traffic_record(wl.name)},
+            "compress_roofline": compress_roofline,
+            "gpu_launches": per_step_launches * steps,
+        },
+    }
+    del cache
+    return res
+
+
+def decode_launches_per_step(splits):
+    """Kernels one snap_decode_step launches (ring append, attention, and the split merge
+    when the plan has more than one split)."""
+    return 3 if splits > 1 else 2
+
+
+def decode_kernel_name(wl):
+    return ("mla_decode_tc_kernel" if wl.layout == 1 else "gqa_decode_kernel") + \
+        " in snap_decode_step (append + split-KV attention + merge), per launch"
+
+
+SUB_WORKLOADS = ["gqa_2k_tiny", "gqa_16k32k_b8", "mla_128k_b8", "gqa_mixed_b64"]
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from fixed_size_kv_gb300 import inputs, snap
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    snap.load(build_if_missing=True)
+
+    wl = inputs.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.replace(batch=args.batch)
+    stream = torch.cuda.Stream(device=dev)
+    r = measure(wl, args, args.steps, args.warmup, dev, stream, world, rank)
+    B, lengths = r["B"], r["lengths"]
 
     # ---------------------------------------------------------------- end to end
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world, reduce_max)
+        e2e = run_e2e(args, wl, lengths, r["pre"], r["q_all"], r["k_all"], r["v_all"], r["cfg"], dev, stream,
+                      world, lambda x: max_over_ranks(x, world, dev))
 
     # ---------------------------------------------------------------- CPU oracle sample
     cpu = None
     if rank == 0 and not args.no_cpu:
-        cpu = cpu_baseline(wl, lengths, pre, q_all, k_all, v_all)
+        cpu = cpu_baseline(wl, lengths, r["pre"], r["q_all"], r["k_all"], r["v_all"])
+    for k in ("pre", "q_all", "k_all", "v_all"):
+        r[k] = None
+    torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- the other workloads, briefly
+    workloads = None
+    if not args.no_workloads and not args.batch and args.workload == "gqa_128k_b16":
+        workloads = {}
+        for name in SUB_WORKLOADS:
+            swl = inputs.WORKLOADS[name]
+            if swl.arrival_every > 0:
+                workloads[name] = mixed_batch(swl, args, dev, world, full_run=False)
+            else:
+                sr = measure(swl, args, 2, 3, dev, stream, world, rank, full_run=False)
+                workloads[name] = {"config": workload_config(swl, sr["B"], sr["lengths"], world),
+                                   "steps": 2, "warmup": 3, "tok_s": sr["value"], "ms_per_step": sr["ms_per_step"],
+                                   "decode_splits": sr["splits"], **sr["fields"]}
+                del sr
+            torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
@@ -430,55 +576,30 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
-    n_seq_launch = 5  # rowstat, lse merge, colsum, select, cache write (scored prompts)
-    per_step_launches = 0
-    for S in lengths:
-        M = (max(wl.L_sink, S - wl.L_recent) if S > wl.L_sink else S) - min(S, wl.L_sink)
-        per_step_launches += n_seq_launch if (M > wl.K and wl.K > 0) else 1
-    # decode launches per step: append, attention, and the split merge when the plan
-    # has more than one split (one split at 16 x 128k GQA: no merge kernel runs)
-    splits = cache.decode_attn_plan(B)[0]
-    per_step_launches += D * (3 if splits > 1 else 2)
-    traffic = traffic_record(wl.name)
+    config = workload_config(wl, B, lengths, world)
+    if r["flush"]:
+        config["l2"] = f"L2 flushed before each step ({2 * L2_BYTES >> 20} MiB write)"
     line = {
         "metric": METRIC,
-        "value": value,
+        "value": r["value"],
         "unit": "tok/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms_step,
+        "ms_per_step": r["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": wl.name, "batch": B, "prompt_len": max(lengths), "decode_steps": D,
-                   "cache": f"{wl.L_sink}+{wl.K}+{wl.L_recent}={wl.C}", "W": wl.W, "P": wl.P,
-                   "heads": f"{wl.n_q_heads}/{wl.n_kv_heads}x{wl.d_qk}",
-                   "parallelism": f"replicas x{world}",
-                   "l2": ("inputs larger than L2 (no flush)" if flush is None
-                          else f"L2 flushed before each step ({2 * L2_BYTES >> 20} MiB write)"),
-                   "decode_launch": "cuda graph" if graph is not None else "eager",
-                   "decode_splits": splits},
-        "decode_tok_s": B * D * world / (dec_ms / 1e3),
-        "decode_ms_per_token_step": dec_ms / D,
-        "compress_ms_per_batch": cmp_ms,
-        "compress_ms_per_seq": cmp_ms / B,
-        "compress_with_prefill_lse_ms_per_seq": cmp_lse_ms,
-        "attn": {"ms": attn_avg_ms, "hbm_gbs": attn_gbs, "bytes_per_launch": attn_bytes},
-        "full_kv": full,
-        "speedup_vs_full_kv": (B * D * world / (dec_ms / 1e3)) / full["decode_tok_s"] if full else None,
-        "cache_bytes": snap.cache_bytes(cfg, B),
-        "roofline": {"bound": "hbm", "kernel": "snap_decode_step (append + split-KV attention + merge)",
-                     "achieved": attn_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": attn_gbs / hbm_peak, "peak_source": peak_kind,
-                     "traffic": traffic},
+        "config": config,
+        "launch": {"decode": "cuda graph" if r["graph"] else "eager", "decode_splits": r["splits"]},
+        **r["fields"],
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": per_step_launches * args.steps,
-        "clocks": clk,
-        "wall_s": t_wall,
+        "workloads": workloads,
+        "clocks": r["clk"],
+        "wall_s": r["t_wall"],
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -604,12 +725,18 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
 
 
 # ----------------------------------------------------------------------------- oracle
-def cpu_sample(wl, lengths, K0, V0, Q0, q1, k1, v1):
+def cpu_sample(wl, lengths, K0, V0, Q0, q1, k1, v1, threads=1):
     """Times the CPU oracle on a bounded sample and scales it to the whole step.
-    Sample: the window scoring of KV head 0 of sequence 0 (the compression's cost,
-    linear in prompt length) over a prompt prefix of at most 16384 tokens, plus
-    max-pool and top-K over it; and one decode step (append + attention) of
-    sequence 0 over a cache of the workload's size."""
+
+    Sample: the window scoring, max-pool and top-K of sequence 0's KV heads over a
+    prompt prefix of at most 16384 tokens (the compression's cost, linear in prompt
+    length), and one decode step (append + attention) over a cache of the workload's
+    size.  threads == 1: one KV head's scoring and one sequence's decode, on one core.
+    threads > 1: every KV head of sequence 0 scored at once and the decode of
+    min(batch, threads) sequences at once, one oracle call per thread (the C oracle
+    releases the GIL; the work per call is unchanged)."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import oracle
     B, D = wl.batch, wl.decode_steps
     oracle.build()
@@ -618,56 +745,92 @@ def cpu_sample(wl, lengths, K0, V0, Q0, q1, k1, v1):
     G = wl.G
     one = wl.replace(n_q_heads=G, n_kv_heads=1)
     ocfg1 = oracle.Config(**one.config_kwargs())
+    # scoring units: (KV head, group of query heads); MLA's 128 heads in groups of 8
+    grp = 8 if G > 8 else G
+    units = [(h, g0) for h in range(wl.n_kv_heads) for g0 in range(0, G, grp)]
+    if threads == 1:
+        units = units[:max(1, G // grp)]         # one KV head: all its query heads
+    sub = oracle.Config(**wl.replace(n_q_heads=grp, n_kv_heads=1).config_kwargs())
+    heads_per_unit_set = len(units) * grp / G       # KV heads covered by the sample
+    K1 = [K0[:S_s, h:h + 1].contiguous() for h in range(wl.n_kv_heads)]
+
+    def score(u):
+        h, g0 = u
+        return oracle.window_scores(sub, K1[h], Q0[:, h * G + g0:h * G + g0 + grp].contiguous())[1][0]
+
     t0 = time.perf_counter()
-    K1 = K0[:S_s, 0:1].contiguous()
-    _, col = oracle.window_scores(ocfg1, K1, Q0[:, 0:G].contiguous())
-    pooled = oracle.maxpool(col[0, :S_s - wl.W], wl.P)
+    with ThreadPoolExecutor(threads) as ex:
+        cols = list(ex.map(score, units))
+    col = sum(cols[:max(1, G // grp)])
+    pooled = oracle.maxpool(col[:S_s - wl.W], wl.P)
     oracle.select(pooled, wl.L_sink, S_s - wl.W, max(1, wl.K * S_s // S_full))  # K scaled to the prefix
     t_c = time.perf_counter() - t0
-    compress_full = t_c * (S_full / S_s) * wl.n_kv_heads * B
-    # decode: a cache of the workload's size built by layout alone (no scoring needed)
+    compress_full = t_c * (S_full / S_s) * (wl.n_kv_heads / heads_per_unit_set) * B
+    # decode: caches of the workload's size built by layout alone (no scoring needed)
     ocfg = oracle.Config(**wl.config_kwargs())
     keep = wl.L_sink + wl.K + wl.L_recent
     Kc = K0[:keep].contiguous()
     Vc = V0[:keep].contiguous() if V0 is not None else None
-    cache = oracle.compress(ocfg, Kc, Vc, Q0)
+    n_dec = 1 if threads == 1 else min(B, threads)
+    caches = [oracle.compress(ocfg, Kc, Vc, Q0) for _ in range(n_dec)]
+
+    def dec(c):
+        oracle.append(c, k1, v1)
+        oracle.decode_attn(c, q1)
+
     t0 = time.perf_counter()
-    oracle.append(cache, k1, v1)
-    oracle.decode_attn(cache, q1)
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(dec, caches))
     t_d = time.perf_counter() - t0
-    decode_full = t_d * B * D
+    decode_full = t_d * (B / n_dec) * D
     total = compress_full + decode_full
-    return {"value": B * D / total, "unit": "tok/s", "cores": 1, "kind": "oracle",
-            "sample": (f"window scoring + pool + top-K of 1 KV head over a {S_s}-token prefix ({t_c:.2f}s, "
-                       f"scaled x{S_full / S_s:.0f} length x{wl.n_kv_heads * B} heads/seqs) + 1 decode step "
-                       f"of 1 sequence ({t_d:.2f}s, scaled x{B * D}); single-threaded C, fp64"),
+    return {"value": B * D / total, "unit": "tok/s", "cores": threads, "kind": "oracle",
+            "sample": (f"window scoring + pool + top-K of {heads_per_unit_set:g} KV head(s) of sequence 0 over a "
+                       f"{S_s}-token prefix ({t_c:.2f}s, scaled x{S_full / S_s:.0f} length, "
+                       f"x{wl.n_kv_heads / heads_per_unit_set * B:g} heads/seqs) + 1 decode step of {n_dec} "
+                       f"sequence(s) ({t_d:.2f}s, scaled x{B / n_dec * D:g}); C oracle in fp64 on {threads} "
+                       f"thread(s)"),
             "seconds": t_c + t_d, "compress_s_est": compress_full, "decode_s_est": decode_full}
 
 
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
 def cpu_baseline(wl, lengths, pre, q_all, k_all, v_all):
+    """The oracle on every host core (the reported baseline), with the one-core run beside it."""
     p0 = pre[0]
-    return cpu_sample(wl, lengths, p0.K.cpu(), p0.V.cpu() if p0.V is not None else None, p0.Q.cpu(),
-                      q_all[0, 0].cpu(), k_all[0, 0].cpu(), v_all[0, 0].cpu() if v_all is not None else None)
+    args = (wl, lengths, p0.K.cpu(), p0.V.cpu() if p0.V is not None else None, p0.Q.cpu(),
+            q_all[0, 0].cpu(), k_all[0, 0].cpu(), v_all[0, 0].cpu() if v_all is not None else None)
+    n = host_cores()
+    multi = cpu_sample(*args, threads=n)
+    single = cpu_sample(*args, threads=1)
+    multi["host_cores"] = n
+    multi["single_thread"] = {"value": single["value"], "cores": 1, "sample": single["sample"]}
+    return multi
 
 
 def run_reference(args):
     """The CPU oracle as the reference arm: each step is one bounded sample of the
-    workload (see cpu_sample), timed on the host cores, scaled to tok/s."""
+    workload (see cpu_sample), timed on every host core, scaled to tok/s."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    import torch
     from fixed_size_kv_gb300 import inputs
     wl = inputs.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.replace(batch=args.batch)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     lengths = inputs.prompt_lengths(wl, args.seed)
     S_s = min(lengths[0], 16384)
     keep = max(S_s, wl.C)
     pre = inputs.gen_prefill(wl, keep, seed=args.seed, seq=0)
     tok = inputs.gen_decode(wl, 1, step=0, seed=args.seed)
+    n = host_cores()
     vals, secs = [], []
     for i in range(args.warmup + args.steps):
         r = cpu_sample(wl, [lengths[0]], pre.K, pre.V, pre.Q, tok.q[0], tok.k[0],
-                       tok.v[0] if tok.v is not None else None)
+                       tok.v[0] if tok.v is not None else None, threads=n)
         if i >= args.warmup:
             vals.append(r["value"])
             secs.append(r["seconds"])
@@ -677,30 +840,24 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": B * D / value * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": wl.name, "batch": B, "prompt_len": lengths[0], "decode_steps": D,
-                       "cache": f"{wl.L_sink}+{wl.K}+{wl.L_recent}={wl.C}"},
-            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "config": workload_config(wl, B, lengths, world),
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": n, "host_cores": n, "kind": "oracle",
                              "sample": r["sample"]},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "sample_seconds_per_step": statistics.mean(secs)}
     print(json.dumps(line), flush=True)
 
 
-def run_mixed(args):
+def mixed_batch(wl, args, dev, world, full_run=True):
     """Continuous batch with arrivals (the 64-slot mixed workload): every
     `arrival_every` decode steps, the slots whose request finished take new requests,
     which are compressed on a second stream while the first keeps decoding the
     others; a new request joins the decode batch at the next arrival boundary.
-    value = decoded tokens / wall time of the whole run (compressions included)."""
+    value = decoded tokens / device time of the whole run (compressions included).
+    Returns the fields of the workload's JSON record."""
     import torch
     from fixed_size_kv_gb300 import inputs, snap
 
-    torch.cuda.set_device(0)
-    dev = torch.device("cuda", 0)
-    snap.load(build_if_missing=True)
-    wl = inputs.WORKLOADS[args.workload]
-    if args.batch:
-        wl = wl.replace(batch=args.batch)
     B, D, every = wl.batch, wl.decode_steps, wl.arrival_every
     sa, sb = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     n_req = B * 16
@@ -783,28 +940,47 @@ def run_mixed(args):
         return tokens, e0.elapsed_time(e1), n_compress, dec_bytes
 
     run(min(D, 64), False)                       # warm-up
-    clocks = ClockSampler(0)
-    clocks.start()
+    clocks = ClockSampler(dev.index or 0) if full_run else None
+    if clocks:
+        clocks.start()
     tokens, ms, n_compress, dec_bytes = run(D, True)
     hbm_peak, _, _, peak_kind = peaks()
     achieved = dec_bytes / (ms / 1e3) / 1e9
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks else None
     st = cache.check_device(sa)
     if st != snap.SNAP_OK:
         raise RuntimeError(f"device status: {snap.status_string(st)}")
-    line = {"metric": METRIC, "value": tokens / (ms / 1e3), "unit": "tok/s", "n_gpus": 1, "steps": D,
-            "warmup": 1, "ms_per_step": ms / D, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "slots": B, "prompt_len": f"U[{wl.prompt_min},{wl.prompt_max}]",
+    del cache, pool, toks
+    return {"config": {"workload": wl.name, "slots": B, "prompt_len": f"U[{wl.prompt_min},{wl.prompt_max}]",
                        "decode_steps": D, "arrival_every": every,
-                       "cache": f"{wl.L_sink}+{wl.K}+{wl.L_recent}={wl.C}",
-                       "output_len": "U[32,1024]", "prompt_pool": NP},
+                       "cache": f"{wl.L_sink}+{wl.K}+{wl.L_recent}={wl.C}", "W": wl.W, "P": wl.P,
+                       "heads": f"{wl.n_q_heads}/{wl.n_kv_heads}x{wl.d_qk}",
+                       "output_len": "U[32,1024]", "prompt_pool": NP, "parallelism": f"replicas x{world}"},
+            "tok_s": tokens / (ms / 1e3), "ms": ms, "ms_per_step": ms / D,
             "decoded_tokens": tokens, "arrivals_compressed": n_compress,
             "roofline": {"bound": "hbm", "kernel": "snap_decode_step over the run (compressions overlap on a "
                          "second stream, so this is a lower bound)", "achieved": achieved, "peak": hbm_peak,
                          "unit": "GB/s", "frac": achieved / hbm_peak, "peak_source": peak_kind,
                          "traffic": None, "decode_bytes": dec_bytes},
             "clocks": clk}
+
+
+def run_mixed(args):
+    """The mixed continuous batch as its own JSON line (python bench.py --workload gqa_mixed_b64)."""
+    import torch
+    from fixed_size_kv_gb300 import inputs, snap
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    snap.load(build_if_missing=True)
+    wl = inputs.WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.replace(batch=args.batch)
+    r = mixed_batch(wl, args, dev, 1)
+    line = {"metric": METRIC, "value": r["tok_s"], "unit": "tok/s", "n_gpus": 1, "steps": wl.decode_steps,
+            "warmup": 1, "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": r["config"],
+            "decoded_tokens": r["decoded_tokens"], "arrivals_compressed": r["arrivals_compressed"],
+            "roofline": r["roofline"], "clocks": r["clocks"]}
     print(json.dumps(line), flush=True)
 
 

@@ -444,10 +444,12 @@ snap_status snap_compress_ws_bytes(const snap_config* cfg, int64_t S_max, size_t
 
 namespace {
 
-// Compression of one sequence; lse_obs (nullable) replaces the row pass.
+// Compression of one sequence, the stages selected by `stages` (SNAP_STAGE_*);
+// lse_obs (nullable) replaces the row pass.
 snap_status compress_impl(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
                           int64_t tok_stride, int64_t head_stride, const void* Q_obs, const float* lse_obs,
-                          void* ws, size_t ws_bytes, void* stream) {
+                          void* ws, size_t ws_bytes, int stages, void* stream) {
+    if (stages & ~SNAP_STAGE_ALL) return SNAP_ERR_INVALID_ARG;
     if (!cache || !K || !Q_obs) return SNAP_ERR_INVALID_ARG;
     const snap_config& c = cache->cfg;
     if (slot < 0 || slot >= cache->max_batch) return SNAP_ERR_INVALID_ARG;
@@ -500,8 +502,9 @@ snap_status compress_impl(snap_cache* cache, int slot, const void* K, const void
         a.S_pad = w.S_pad;
         a.R_pad = w.R_pad;
         ScoreParams sp = score_params(c, S, w, wb, cache->status);
-        cudaError_t e;
-        if (lse_obs) {
+        cudaError_t e = cudaSuccess;
+        if (!(stages & SNAP_STAGE_ROWS)) {
+        } else if (lse_obs) {
             // 1-2. the caller's row log-sum-exp, in the base-2 domain the GEMM uses
             e = launch_lse_import(a, lse_obs, st);
         } else {
@@ -514,7 +517,7 @@ snap_status compress_impl(snap_cache* cache, int slot, const void* K, const void
             }
         }
         // 3. column pass: X = 128-key tiles, Y = observation rows
-        if (e == cudaSuccess) {
+        if (e == cudaSuccess && (stages & SNAP_STAGE_COLUMNS)) {
             CUtensorMap tx, ty;
             const int nx = (int)((S - c.W + 127) / 128);
             const int ny64 = (w.R + 63) / 64 * 64;
@@ -535,9 +538,10 @@ snap_status compress_impl(snap_cache* cache, int slot, const void* K, const void
             e = launch_score_tc(SCORE_COLSUM, tx, ty, sp, c.d_qk, false, !y_resident, num_sms(), st);
         }
         // 4. pool + top-K
-        if (e == cudaSuccess) e = launch_select(a, st);
+        if (e == cudaSuccess && (stages & SNAP_STAGE_SELECT)) e = launch_select(a, st);
         if (e != cudaSuccess) return cuda_status(e);
     }
+    if (!(stages & SNAP_STAGE_WRITE)) return SNAP_OK;
     return cuda_status(launch_cache_write(a, num_sms(), st));
 }
 
@@ -548,14 +552,24 @@ extern "C" {
 snap_status snap_compress(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
                           int64_t tok_stride, int64_t head_stride, const void* Q_obs, void* ws,
                           size_t ws_bytes, void* stream) {
-    return compress_impl(cache, slot, K, V, S, tok_stride, head_stride, Q_obs, nullptr, ws, ws_bytes, stream);
+    return compress_impl(cache, slot, K, V, S, tok_stride, head_stride, Q_obs, nullptr, ws, ws_bytes,
+                         SNAP_STAGE_ALL, stream);
+}
+
+snap_status snap_compress_stages(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
+                                 int64_t tok_stride, int64_t head_stride, const void* Q_obs, const float* lse_obs,
+                                 void* ws, size_t ws_bytes, int stages, void* stream) {
+    if (lse_obs && (reinterpret_cast<uintptr_t>(lse_obs) & 3u)) return SNAP_ERR_INVALID_ARG;
+    return compress_impl(cache, slot, K, V, S, tok_stride, head_stride, Q_obs, lse_obs, ws, ws_bytes, stages,
+                         stream);
 }
 
 snap_status snap_compress_lse(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
                               int64_t tok_stride, int64_t head_stride, const void* Q_obs, const float* lse_obs,
                               void* ws, size_t ws_bytes, void* stream) {
     if (!lse_obs || (reinterpret_cast<uintptr_t>(lse_obs) & 3u)) return SNAP_ERR_INVALID_ARG;
-    return compress_impl(cache, slot, K, V, S, tok_stride, head_stride, Q_obs, lse_obs, ws, ws_bytes, stream);
+    return compress_impl(cache, slot, K, V, S, tok_stride, head_stride, Q_obs, lse_obs, ws, ws_bytes,
+                         SNAP_STAGE_ALL, stream);
 }
 
 snap_status snap_window_logits(snap_cache* cache, const void* K, int64_t S, int64_t tok_stride,

@@ -26,6 +26,12 @@ SNAP_ERR_DEVICE_CHECK = 6
 LAYOUT_GQA = 0
 LAYOUT_MLA = 1
 
+STAGE_ROWS = 1
+STAGE_COLUMNS = 2
+STAGE_SELECT = 4
+STAGE_WRITE = 8
+STAGE_ALL = 15
+
 
 class SnapError(RuntimeError):
     def __init__(self, status: int, where: str):
@@ -59,6 +65,7 @@ SIGNATURES = {
     "snap_compress_ws_bytes": (_I, [_P(snap_config), _I64, _P(_SZ)]),
     "snap_compress": (_I, [_VP, _I, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _SZ, _VP]),
     "snap_compress_lse": (_I, [_VP, _I, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _SZ, _VP]),
+    "snap_compress_stages": (_I, [_VP, _I, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _SZ, _I, _VP]),
     "snap_window_logits": (_I, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP]),
     "snap_decode_append": (_I, [_VP, _VP, _I, _VP, _VP, _VP]),
     "snap_decode_attn_ws_bytes": (_I, [_P(snap_config), _I, _P(_SZ)]),
@@ -221,6 +228,19 @@ class SnapCache:
         _check(load().snap_compress_lse(self.handle, slot, _ptr(K), _ptr(V), S, K.stride(0), K.stride(1),
                                         _ptr(Q_obs), _ptr(lse_obs), _ptr(self.ws_compress),
                                         self.ws_compress.numel(), _stream(stream)), "snap_compress_lse")
+
+    def compress_stages(self, slot: int, K: torch.Tensor, V: torch.Tensor | None, Q_obs: torch.Tensor,
+                        stages: int, lse_obs: torch.Tensor | None = None, stream=None) -> None:
+        """snap_compress_stages: only the stages in `stages` (STAGE_* bits), in order."""
+        S = K.shape[0]
+        self.ensure_compress_ws(S)
+        if lse_obs is not None:
+            assert lse_obs.dtype == torch.float32 and lse_obs.is_contiguous()
+        Q_obs = Q_obs.contiguous()
+        _check(load().snap_compress_stages(self.handle, slot, _ptr(K), _ptr(V), S, K.stride(0), K.stride(1),
+                                           _ptr(Q_obs), _ptr(lse_obs), _ptr(self.ws_compress),
+                                           self.ws_compress.numel(), int(stages), _stream(stream)),
+               "snap_compress_stages")
 
     def window_logits(self, K: torch.Tensor, Q_obs: torch.Tensor, stream=None) -> torch.Tensor:
         """Base-2 logits of the observation rows against every prompt key:

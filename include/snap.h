@@ -168,6 +168,30 @@ snap_status snap_compress_lse(snap_cache* cache, int slot, const void* K, const 
                               int64_t tok_stride, int64_t head_stride, const void* Q_obs, const float* lse_obs,
                               void* ws, size_t ws_bytes, void* stream);
 
+/* Stages of a compression, in the order they run (snap_compress_stages). */
+enum {
+    SNAP_STAGE_ROWS = 1,     /* row pass: log-sum-exp of every observation row (or import of lse_obs) */
+    SNAP_STAGE_COLUMNS = 2,  /* column pass: per prompt position, the window softmax summed over rows */
+    SNAP_STAGE_SELECT = 4,   /* max-pool of width P and top-K of the middle positions */
+    SNAP_STAGE_WRITE = 8,    /* cache build: sinks, selected rows, ring; sequence meta */
+    SNAP_STAGE_ALL = 15
+};
+
+/*
+ * snap_compress() (lse_obs NULL) or snap_compress_lse() (lse_obs given), running only
+ * the stages set in `stages`.  The stages hand their results to the next one through
+ * the workspace `ws` and the cache's selection list, so running every stage in order,
+ * in one call or in several calls on the same stream with the same arguments and
+ * workspace, gives exactly the result of the one-call form.  For profiling the steps
+ * of the "Fixed-Size Cache Layout" build (score passes, pooling + top-K, cache write)
+ * one at a time, and for callers that interleave the stages of several sequences.
+ * When the prompt needs no scoring (the middle holds <= K positions) only the write
+ * stage does anything.  SNAP_ERR_INVALID_ARG for bits outside SNAP_STAGE_ALL.
+ */
+snap_status snap_compress_stages(snap_cache* cache, int slot, const void* K, const void* V, int64_t S,
+                                 int64_t tok_stride, int64_t head_stride, const void* Q_obs,
+                                 const float* lse_obs, void* ws, size_t ws_bytes, int stages, void* stream);
+
 /*
  * Inspection of the compression's score GEMM: the base-2 logits
  * out[h][r][j] = log2(e) * sm_scale * q_r . k_j  (fp32 [n_kv_heads][G*W][S]) of every

@@ -157,3 +157,36 @@ def test_compress_with_supplied_lse_matches_oracle(mla):
     assert cache.check_device() == snap.SNAP_OK
     ocache = oracle.compress(oracle_cfg(wl), pre.K, pre.V, pre.Q, want_pool=True)
     check_all(wl, pre, cache, ocache, where="supplied lse")
+
+
+@pytest.mark.parametrize("mla", [False, True])
+def test_compress_stage_by_stage_equals_one_call(mla):
+    """snap_compress_stages: the four stages run as four calls on one stream give the
+    one-call result bit for bit (selection, every cache row, meta); a call without the
+    write stage leaves the cache untouched."""
+    if mla:
+        wl = inputs.Workload("mla_small", 1, 128, 1, 576, 512, 4, 40, 64, 4, 5, 1, 0, 0, 0,
+                             1 / math.sqrt(192))
+        S = 900
+    else:
+        wl = small_gqa(K=124, L_recent=128)
+        S = 3000
+    pre = inputs.gen_prefill(wl, S, seed=41)
+    K, V, Q = pre.K.cuda(), (pre.V.cuda() if pre.V is not None else None), pre.Q.cuda()
+    one = snap.SnapCache(snap_cfg(wl), max_batch=1, max_prompt=S)
+    one.compress(0, K, V, Q)
+    staged = snap.SnapCache(snap_cfg(wl), max_batch=1, max_prompt=S)
+    staged.compress_stages(0, K, V, Q, snap.STAGE_ROWS | snap.STAGE_COLUMNS | snap.STAGE_SELECT)
+    torch.cuda.synchronize()
+    assert float(staged.k_cache().float().abs().sum()) == 0.0      # nothing written yet
+    for st in (snap.STAGE_ROWS, snap.STAGE_COLUMNS, snap.STAGE_SELECT, snap.STAGE_WRITE):
+        staged.compress_stages(0, K, V, Q, st)
+    torch.cuda.synchronize()
+    assert one.check_device() == snap.SNAP_OK and staged.check_device() == snap.SNAP_OK
+    assert torch.equal(one.selected(), staged.selected())
+    assert torch.equal(one.k_cache(), staged.k_cache())
+    if V is not None:
+        assert torch.equal(one.v_cache(), staged.v_cache())
+    assert torch.equal(one.meta(), staged.meta())
+    ocache = oracle.compress(oracle_cfg(wl), pre.K, pre.V, pre.Q, want_pool=True)
+    check_all(wl, pre, staged, ocache, where="staged")
