@@ -16,10 +16,11 @@
 // Per 64-key tile: S into TMEM with N = 64 score MMAs (q's four chunks 0..3 from
 // TMEM, chunks 4..8 from shared memory), the softmax, the bf16 weights P written
 // over their scores in TMEM, then O += P V as one N = 256 MMA per 16 keys (the
-// CTA's four 64-column value chunks, 8 KB apart in the stage).  A tcgen05.mma with
-// a small N costs about as much as one with N = 64, so the instruction count per
-// key sets the pace.  TMEM columns: scores / weights 0..127 (one 64-column buffer
-// per softmax group), q 128..255, O 256..511.
+// CTA's four 64-column value chunks, 8 KB apart in the stage).  Measured on GB300
+// with back-to-back issue: an M = 128 tcgen05.mma takes ~45 cycles at any N <= 64,
+// 64 at N = 128 and 128 at N = 256 (4096 MAC/clk), so the 36 N = 64 score MMAs of a
+// tile run at about 70% of the tensor rate.  TMEM columns: scores / weights 0..127
+// (one 64-column buffer per softmax group), q 128..255, O 256..511.
 //
 // Roles (320 threads per CTA): warp 0 issues TMA loads (and L2 prefetches ahead),
 // warp 1 owns TMEM and one thread issues tcgen05.mma from two queues (scores of the
@@ -174,6 +175,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0 && t_begin < t_end) {
             const uint32_t id_qk = idesc_bf16(HEADS, TK);
             const uint32_t id_pv = idesc_bf16_bmn(HEADS, 256);   // this CTA's four value chunks per MMA
+            // Descriptors are formed once; the MMAs of a tile add compile-time offsets to
+            // their start-address field (16-byte units), so the issuing thread spends a
+            // few instructions per MMA (a tcgen05.mma takes ~45 cycles at N = 64).
+            const uint64_t q_desc = desc_sw128(s_q);
+            const uint64_t kv_desc0 = desc_sw128(s_kv);
+            const uint64_t v_desc0 = desc_sw128_mn(s_kv + 4 * half * CH_B, CH_B);
+            constexpr uint64_t CH16 = CH_B >> 4, QCH16 = QCH_B >> 4, ST16 = (NCH * CH_B) >> 4;
             bool ok = wait_bar(bar(B_Q_FULL), 0, abort_flag);
             if (!ok) fail(10);
             // Two queues: P V of the oldest tile with weights ready (first: it frees a
@@ -189,11 +197,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_after();
                     const int stp = pv % KST;
                     const uint32_t pa = T_S + (pv & 1) * TK;  // the weights, written over the scores
-                    const uint32_t vb = s_kv + (stp * NCH + 4 * half) * CH_B;
+                    const uint64_t vd = v_desc0 + (uint64_t)stp * ST16;
+                    tc_mma_ta(T_O, pa, vd, id_pv, pv > 0 ? 1u : 0u);
 #pragma unroll
-                    for (int k = 0; k < TK / 16; ++k)       // 16 keys (8 TMEM columns of P) per step
-                        tc_mma_ta(T_O, pa + k * 8, desc_sw128_mn(vb + k * 2048, CH_B), id_pv,
-                                  (pv > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 1; k < TK / 16; ++k)       // 16 keys (8 TMEM columns of P) per step
+                        tc_mma_ta(T_O, pa + k * 8, vd + (uint64_t)k * (2048 >> 4), id_pv, 1u);
                     tc_commit(bar(B_SP_EMPTY + (pv & 1)));
                     tc_commit(bar(B_KV_EMPTY + stp));
                     ++pv;
@@ -204,16 +212,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_after();
                     const int st = qk % KST, sb = qk & 1;
                     const uint32_t d = T_S + sb * TK;
-                    for (int j = 0; j < QT_CH; ++j)     // q chunks 0..3 from TMEM
+                    const uint64_t kd = kv_desc0 + (uint64_t)st * ST16;
+                    tc_mma_ta(d, T_Q, kd, id_qk, 0u);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)     // 16 columns (8 TMEM columns of q) per step
-                            tc_mma_ta(d, T_Q + j * 32 + k * 8, desc_sw128(s_kv + (st * NCH + j) * CH_B + k * 32),
-                                      id_qk, (j | k) ? 1u : 0u);
-                    for (int j = QT_CH; j < NCH; ++j)   // q chunks 4..8 from shared memory
+                    for (int i = 1; i < 4 * QT_CH; ++i)      // q chunks 0..3 from TMEM; 16 columns
+                        tc_mma_ta(d, T_Q + (i >> 2) * 32 + (i & 3) * 8,   // (8 TMEM columns of q) per step
+                                  kd + (uint64_t)((i >> 2) * CH16 + (i & 3) * 2), id_qk, 1u);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            tc_mma(d, desc_sw128(s_q + (j - QT_CH) * QCH_B + k * 32),
-                                   desc_sw128(s_kv + (st * NCH + j) * CH_B + k * 32), id_qk, 1u);
+                    for (int i = 4 * QT_CH; i < 4 * NCH; ++i) // q chunks 4..8 from shared memory
+                        tc_mma(d, q_desc + (uint64_t)(((i >> 2) - QT_CH) * QCH16 + (i & 3) * 2),
+                               kd + (uint64_t)((i >> 2) * CH16 + (i & 3) * 2), id_qk, 1u);
                     tc_commit(bar(B_S_FULL + sb));
                     ++qk;
                     progressed = true;
