@@ -471,7 +471,7 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
     for S in lengths:
         M = (max(wl.L_sink, S - wl.L_recent) if S > wl.L_sink else S) - min(S, wl.L_sink)
         per_step_launches += n_seq_launch if (M > wl.K and wl.K > 0) else 1
-    per_step_launches += D * decode_launches_per_step(splits)
+    per_step_launches += D * decode_launches_per_step(wl, splits)
     res = {
         "lengths": lengths, "pre": pre, "q_all": q_all, "k_all": k_all, "v_all": v_all, "cfg": cfg,
         "B": B, "D": D, "steps": steps, "graph": graph is not None, "flush": flush is not None,
@@ -504,15 +504,18 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
     return res
 
 
-def decode_launches_per_step(splits):
-    """Kernels one snap_decode_step launches (ring append, attention, and the split merge
-    when the plan has more than one split)."""
-    return 3 if splits > 1 else 2
+def decode_launches_per_step(wl, splits):
+    """Kernels one snap_decode_step launches: GQA one (ring append, attention and split
+    merge fused); MLA the attention (with the append) plus the merge when it splits."""
+    if wl.layout == 0:
+        return 1
+    return 2 if splits > 1 else 1
 
 
 def decode_kernel_name(wl):
-    return ("mla_decode_tc_kernel" if wl.layout == 1 else "gqa_decode_kernel") + \
-        " in snap_decode_step (append + split-KV attention + merge), per launch"
+    if wl.layout == 0:
+        return "gqa_decode_kernel = snap_decode_step (ring append + split-KV attention + split merge), per launch"
+    return "mla_decode_tc_kernel in snap_decode_step (ring append + split-KV attention; merge kernel after), per step"
 
 
 SUB_WORKLOADS = ["gqa_2k_tiny", "gqa_16k32k_b8", "mla_128k_b8", "gqa_mixed_b64"]

@@ -3,10 +3,14 @@
 // SnapStream episode companion page, "Prefill / Decode Pipeline": decode is
 // memory-bound, so the cache bytes streamed per step set the time per token.
 // GQA: each CTA streams one contiguous range of cache slots of one (sequence, KV head)
-// once from HBM and produces an un-normalised partial (max, sum, O) per query
-// head; a merge kernel combines the splits (flash-decoding's log-sum-exp merge).
-// Invalid slots (unused middle slots, ring slots not holding a live position)
-// are masked; whole tiles with no valid slot are not read.
+// once from HBM and produces an un-normalised partial (max, sum, O) per query head;
+// the last CTA of a (sequence, KV head) to finish combines the splits (flash-decoding's
+// log-sum-exp merge), so a decode step is one launch.  The ring append of the step
+// ("Ring Buffer vs. Naive Slicing": scatter the new token into its fixed ring slot) is
+// fused in: the CTA whose key range holds the slot writes the new row before reading.
+// Invalid slots (unused middle slots, ring slots not holding a live position) are
+// masked; whole tiles with no valid slot are not read.  The MLA layout's split merge
+// runs as its own kernel (decode_merge_kernel): 128 heads x 512 values per sequence.
 #include "kernels.cuh"
 
 namespace snap {
@@ -27,9 +31,11 @@ constexpr int G_STAGE_BYTES = GQA_KEYS * G_ROWB * 2;        // K + V tile = 16 K
 constexpr int G_SMEM = G_WARPS * G_STAGES * G_STAGE_BYTES;  // 192 KB
 
 __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs a) {
-    pdl_wait();                 // the append (or whatever produced q) has completed
-    pdl_launch_dependents();    // the merge may launch once the last wave has started
+    pdl_wait();                 // the previous kernel on the stream has completed
+    pdl_launch_dependents();    // the next step's kernel may set up (it waits for this grid)
     extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ snap_seq_meta m_sh;
+    __shared__ int last_sh;
     const DevConfig& c = a.cfg;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -37,17 +43,46 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
     if (slot < 0 || slot >= c.max_batch) {
         if (threadIdx.x == 0 && split == 0 && h == 0)
             report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
-        if (a.splits == 1)  // otherwise the merge kernel writes the zeros
+        if (split == 0)  // no CTA of this sequence goes on: split 0 writes the zero output
             for (int i = threadIdx.x; i < c.G * GD; i += blockDim.x)
                 a.out[((size_t)b * c.Hq + (size_t)h * c.G) * GD + i] = 0.f;
         return;
     }
-    const snap_seq_meta m = a.meta[slot];
-    SlotValidity sv;
-    sv.init(m, c);
+    if (threadIdx.x == 0) m_sh = a.meta[slot];
+    __syncthreads();
+    snap_seq_meta m = m_sh;
     const size_t row0 = ((size_t)slot * c.Hkv + h) * (size_t)c.C;
     const bf16* kbase = a.kc + row0 * GD;
     const bf16* vbase = a.vc + row0 * GD;
+    const int ntiles = (c.C + GQA_KEYS - 1) / GQA_KEYS;
+    const int t_begin = split * a.tiles_per_split;
+    const int t_end = min(ntiles, t_begin + a.tiles_per_split);
+    if (a.k_new) {
+        // fused ring append: the CTA whose key range holds the new token's ring slot
+        // writes its K/V row before reading any tile; the attention then sees T + 1
+        const int s_app = c.L_sink + c.K + m.T % c.L_recent;
+        if (s_app >= t_begin * GQA_KEYS && s_app < t_end * GQA_KEYS && threadIdx.x < 32) {
+            const bool isv = threadIdx.x >= 16;
+            const int ch = threadIdx.x & 15;
+            const uint4* src = reinterpret_cast<const uint4*>((isv ? a.v_new : a.k_new) + ((size_t)b * c.Hkv + h) * GD);
+            bf16* dst = const_cast<bf16*>(isv ? vbase : kbase) + (size_t)s_app * GD;
+            reinterpret_cast<uint4*>(dst)[ch] = src[ch];
+            __threadfence();
+        }
+        m.T += 1;
+        __syncthreads();
+        // the last CTA of the sequence to get here (every CTA has read the meta) advances T
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const int total = gridDim.x * gridDim.y;   // splits x KV heads
+            if (atomicAdd(&a.meta_rw[slot].pad[0], 1) == total - 1) {
+                a.meta_rw[slot].T = m.T;
+                a.meta_rw[slot].pad[0] = 0;
+            }
+        }
+    }
+    SlotValidity sv;
+    sv.init(m, c);
 
     // Q^T as B fragments: n = head (lane/4), k = d.
     uint32_t qf[8][2];
@@ -65,9 +100,6 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
         }
     }
 
-    const int ntiles = (c.C + GQA_KEYS - 1) / GQA_KEYS;
-    const int t_begin = split * a.tiles_per_split;
-    const int t_end = min(ntiles, t_begin + a.tiles_per_split);
     const uint32_t wsm = smem_u32(smem) + warp * G_STAGES * G_STAGE_BYTES;
 
     auto next_tile = [&](int t) {
@@ -250,6 +282,37 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
                 a.part_ml[pi * 2 + 1] = L;
             }
         }
+    }
+    if (a.splits == 1) return;
+    // split merge in the last CTA of (sequence, KV head) to finish: flash-decoding's
+    // log-sum-exp merge of every split's (max, sum, O) of the G query heads
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int* cnt = a.merge_cnt + (size_t)slot * c.Hkv + h;
+        const int last = atomicAdd(cnt, 1) == a.splits - 1;
+        if (last) *cnt = 0;      // every other CTA has counted: ready for the next call
+        last_sh = last;
+    }
+    __syncthreads();
+    if (!last_sh) return;
+    __threadfence();
+    const size_t p0 = ((size_t)b * c.Hkv + h) * a.splits;
+    for (int hh = 0; hh < c.G; ++hh) {
+        float M = NEG_INF;
+        for (int s2 = 0; s2 < a.splits; ++s2) M = fmaxf(M, __ldcg(a.part_ml + ((p0 + s2) * c.G + hh) * 2));
+        float L = 0.f, O = 0.f;
+        if (M != NEG_INF) {
+            for (int s2 = 0; s2 < a.splits; ++s2) {
+                const size_t pi = (p0 + s2) * c.G + hh;
+                const float mm = __ldcg(a.part_ml + pi * 2);
+                if (mm == NEG_INF) continue;
+                const float w = ex2(mm - M);
+                L += w * __ldcg(a.part_ml + pi * 2 + 1);
+                O += w * __ldcg(a.part_o + pi * GD + d);
+            }
+        }
+        a.out[((size_t)b * c.Hq + (size_t)h * c.G + hh) * GD + d] = L > 0.f ? O / L : 0.f;
     }
 }
 

@@ -138,13 +138,33 @@ __global__ void __launch_bounds__(THREADS, 1)
     snap_seq_meta m{};
     if (slot_ok) {
         m = a.meta[slot];
-        sv.init(m, c);
     } else if (threadIdx.x == 0 && split == 0 && half == 0) {
         report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
     }
     const int ntiles = (c.C + TK - 1) / TK;
     const int t_begin = split * a.tiles_per_split;
     const int t_end = slot_ok ? min(ntiles, t_begin + a.tiles_per_split) : t_begin;
+    if (slot_ok && a.k_new) {
+        // fused ring append: both CTAs of the split whose key range holds the new token's
+        // ring slot write its row (the same bytes) before their own TMA reads of the cache
+        const int s_app = c.L_sink + c.K + m.T % c.L_recent;
+        if (s_app >= t_begin * TK && s_app < t_end * TK && threadIdx.x < c.dqk / 8) {
+            const uint4* src = reinterpret_cast<const uint4*>(a.k_new + (size_t)b * c.dqk);
+            bf16* dst = const_cast<bf16*>(a.kc) + ((size_t)slot * c.C + s_app) * c.dqk;
+            reinterpret_cast<uint4*>(dst)[threadIdx.x] = src[threadIdx.x];
+            asm volatile("fence.proxy.async.global;\n" ::: "memory");   // visible to this CTA's TMA
+        }
+        m.T += 1;
+        __syncthreads();            // every thread has read the meta; the row is written
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(&a.meta_rw[slot].pad[0], 1) == (int)gridDim.x - 1) {   // 2 x splits CTAs
+                a.meta_rw[slot].T = m.T;
+                a.meta_rw[slot].pad[0] = 0;
+            }
+        }
+    }
+    if (slot_ok) sv.init(m, c);
     auto next_tile = [&](int t) {
         while (t < t_end && !sv.any_valid(t * TK, min(c.C, (t + 1) * TK))) ++t;
         return t;

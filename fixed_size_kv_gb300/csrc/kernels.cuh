@@ -27,6 +27,14 @@ struct DecodeArgs {
     int tiles_per_split;         // in units of the kernel's key tile
     int32_t* status;
     DevConfig cfg;
+    // fused ring append (snap_decode_step): the new token of sequence b is written into
+    // ring slot L_sink + K + (T mod L_recent) by the CTA(s) whose key range holds it, the
+    // attention sees T + 1 tokens, and the last CTA of the sequence to finish advances
+    // meta.T (meta.pad[0] counts the CTAs of the sequence that have read the meta)
+    const bf16* k_new;           // [n][Hkv][dqk] or null (no append)
+    const bf16* v_new;           // [n][Hkv][dv] (GQA)
+    snap_seq_meta* meta_rw;      // the same meta, writable (append only)
+    int32_t* merge_cnt;          // [max_batch][Hkv] CTAs of (slot, head) done; zero between calls
 };
 
 constexpr int GQA_KEYS = 32;     // keys per warp step of the GQA decode kernel

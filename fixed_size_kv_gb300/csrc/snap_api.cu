@@ -22,6 +22,7 @@ struct snap_cache {
     snap_seq_meta* meta;
     int32_t* sel;
     int32_t* status;
+    int32_t* merge_cnt;   // [max_batch][n_kv_heads] split-merge arrival counts (zero between calls)
 };
 
 namespace {
@@ -34,19 +35,19 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// SMs of the current device (cached per device).  If the query fails, 1: the plans
-// built from it stay valid (the persistent kernels loop over their units), and the
-// failure itself surfaces at the next launch.
+// SMs of the current device (cached per device); 0 if the query fails.  Every entry
+// point that plans launches checks it first (SNAP_ERR_CUDA), so the helpers below
+// only see a positive count.
 int num_sms() {
     static std::atomic<int> cached[64];     // zero-initialised (static storage)
     int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     const bool cacheable = dev >= 0 && dev < 64;
     if (cacheable) {
         const int c = cached[dev].load(std::memory_order_relaxed);
         if (c > 0) return c;
     }
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
     if (cacheable) cached[dev].store(n, std::memory_order_relaxed);
     return n;
 }
@@ -72,7 +73,7 @@ DevConfig dev_config(const snap_config& c, int max_batch) {
 }
 
 struct CacheRegions {
-    size_t meta, status, sel, k, v, total;
+    size_t meta, status, cnt, sel, k, v, total;
 };
 
 CacheRegions regions(const snap_config& c, int max_batch) {
@@ -83,6 +84,8 @@ CacheRegions regions(const snap_config& c, int max_batch) {
     off = align_up(off + sizeof(snap_seq_meta) * max_batch, 256);
     r.status = off;
     off = align_up(off + 16, 256);
+    r.cnt = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)max_batch * c.n_kv_heads, 256);
     r.sel = off;
     off = align_up(off + sizeof(int32_t) * (size_t)max_batch * c.n_kv_heads * c.K, 256);
     r.k = off;
@@ -346,17 +349,65 @@ bool mla_cache_map(CUtensorMap* tkv, const snap_cache* cache) {
     return encode(tkv, cache->k, 3, kd, ks, kb);
 }
 
+// GQA: one kernel (append, attention, split merge); MLA: the attention kernel (with the
+// append) and, when the plan splits the keys, the merge kernel.
 cudaError_t run_decode(snap_cache* cache, DecodeArgs& a, cudaStream_t st) {
-    cudaError_t e;
-    if (cache->cfg.layout == SNAP_LAYOUT_GQA) {
-        e = launch_decode_gqa(a, st);
-    } else {
-        CUtensorMap tkv;
-        if (!mla_cache_map(&tkv, cache)) return cudaErrorInvalidValue;
-        e = launch_decode_mla_tc(a, tkv, st);
-    }
+    a.meta_rw = cache->meta;
+    a.merge_cnt = cache->merge_cnt;
+    if (cache->cfg.layout == SNAP_LAYOUT_GQA) return launch_decode_gqa(a, st);
+    CUtensorMap tkv;
+    if (!mla_cache_map(&tkv, cache)) return cudaErrorInvalidValue;
+    cudaError_t e = launch_decode_mla_tc(a, tkv, st);
     if (e == cudaSuccess && a.splits > 1) e = launch_decode_merge(a, st);
     return e;
+}
+
+// Arguments shared by the decode-attention entry points (plan, workspace aside).
+snap_status decode_args(snap_cache* cache, const int32_t* slots, int n, const void* q, void* out,
+                        const void* k_new, const void* v_new, DecodeArgs* a) {
+    if (!slots || !q || !out || !aligned16(q) || !aligned16(out)) return SNAP_ERR_INVALID_ARG;
+    if (n > cache->max_batch) return SNAP_ERR_INVALID_ARG;
+    if (num_sms() <= 0) return SNAP_ERR_CUDA;
+    const snap_config& c = cache->cfg;
+    if (k_new) {
+        if (!aligned16(k_new)) return SNAP_ERR_INVALID_ARG;
+        if (c.layout == SNAP_LAYOUT_GQA && (!v_new || !aligned16(v_new))) return SNAP_ERR_INVALID_ARG;
+        if (c.layout == SNAP_LAYOUT_MLA && v_new) return SNAP_ERR_INVALID_ARG;
+    }
+    std::memset(a, 0, sizeof *a);
+    a->kc = cache->k;
+    a->vc = cache->v;
+    a->meta = cache->meta;
+    a->slots = slots;
+    a->n = n;
+    a->q = static_cast<const bf16*>(q);
+    a->out = static_cast<float*>(out);
+    a->status = cache->status;
+    a->cfg = dev_config(c, cache->max_batch);
+    a->k_new = static_cast<const bf16*>(k_new);
+    a->v_new = static_cast<const bf16*>(v_new);
+    int splits = 1;
+    decode_plan(cache, n, &splits, &a->tiles_per_split);
+    a->splits = splits;
+    return SNAP_OK;
+}
+
+// Decode attention (with the fused append when k_new is given) using the caller's workspace.
+snap_status decode_with_ws(snap_cache* cache, const int32_t* slots, int n, const void* q, const void* k_new,
+                           const void* v_new, void* out, void* ws, size_t ws_bytes, void* stream) {
+    if (!cache || n < 0) return SNAP_ERR_INVALID_ARG;
+    if (n == 0) return SNAP_OK;
+    DecodeArgs a;
+    if (const snap_status s = decode_args(cache, slots, n, q, out, k_new, v_new, &a); s != SNAP_OK) return s;
+    const snap_config& c = cache->cfg;
+    if (a.splits > 1) {
+        const size_t need = decode_ws_bytes(c, n);
+        if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SNAP_ERR_INVALID_ARG;
+        const size_t parts = (size_t)n * c.n_q_heads * MAX_DECODE_SPLITS;
+        a.part_o = static_cast<float*>(ws);
+        a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align_up(parts * sizeof(float) * c.d_v, 256));
+    }
+    return cuda_status(run_decode(cache, a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -406,6 +457,7 @@ snap_status snap_cache_create(const snap_config* cfg, int max_batch, void* dev_b
     c->bytes = bytes;
     c->meta = reinterpret_cast<snap_seq_meta*>(base + r.meta);
     c->status = reinterpret_cast<int32_t*>(base + r.status);
+    c->merge_cnt = reinterpret_cast<int32_t*>(base + r.cnt);
     c->sel = reinterpret_cast<int32_t*>(base + r.sel);
     c->k = reinterpret_cast<bf16*>(base + r.k);
     c->v = cfg->layout == SNAP_LAYOUT_GQA ? reinterpret_cast<bf16*>(base + r.v) : nullptr;
@@ -450,6 +502,7 @@ snap_status compress_impl(snap_cache* cache, int slot, const void* K, const void
                           int64_t tok_stride, int64_t head_stride, const void* Q_obs, const float* lse_obs,
                           void* ws, size_t ws_bytes, int stages, void* stream) {
     if (stages & ~SNAP_STAGE_ALL) return SNAP_ERR_INVALID_ARG;
+    if (num_sms() <= 0) return SNAP_ERR_CUDA;
     if (!cache || !K || !Q_obs) return SNAP_ERR_INVALID_ARG;
     const snap_config& c = cache->cfg;
     if (slot < 0 || slot >= cache->max_batch) return SNAP_ERR_INVALID_ARG;
@@ -581,6 +634,7 @@ snap_status snap_window_logits(snap_cache* cache, const void* K, int64_t S, int6
     if (tok_stride < c.d_qk || (tok_stride * 2) % 16 || head_stride < 0 || (head_stride * 2) % 16)
         return SNAP_ERR_INVALID_ARG;
     if (c.n_kv_heads > 1 && head_stride < c.d_qk) return SNAP_ERR_INVALID_ARG;
+    if (num_sms() <= 0) return SNAP_ERR_CUDA;
     const CompressWs w = compress_ws(c, S);
     ScoreParams sp = score_params(c, S, w, nullptr, cache->status);
     sp.logits = out;
@@ -621,8 +675,7 @@ snap_status snap_decode_attn_ws_bytes(const snap_config* cfg, int max_n, size_t*
 snap_status snap_decode_attn_plan(const snap_cache* cache, int n, int* splits, int* tiles_per_split,
                                   int* ctas_per_wave) {
     if (!cache || n < 1 || !splits || !tiles_per_split || !ctas_per_wave) return SNAP_ERR_INVALID_ARG;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SNAP_ERR_CUDA;
+    if (num_sms() <= 0) return SNAP_ERR_CUDA;
     decode_plan(cache, n, splits, tiles_per_split);
     *ctas_per_wave = decode_wave_ctas(cache);
     return SNAP_OK;
@@ -630,39 +683,13 @@ snap_status snap_decode_attn_plan(const snap_cache* cache, int n, int* splits, i
 
 snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, const void* q,
                              void* out, void* ws, size_t ws_bytes, void* stream) {
-    if (!cache || n < 0) return SNAP_ERR_INVALID_ARG;
-    if (n == 0) return SNAP_OK;
-    if (!slots || !q || !out || !aligned16(q) || !aligned16(out)) return SNAP_ERR_INVALID_ARG;
-    if (n > cache->max_batch) return SNAP_ERR_INVALID_ARG;
-    const snap_config& c = cache->cfg;
-    DecodeArgs a;
-    std::memset(&a, 0, sizeof a);
-    a.kc = cache->k;
-    a.vc = cache->v;
-    a.meta = cache->meta;
-    a.slots = slots;
-    a.n = n;
-    a.q = static_cast<const bf16*>(q);
-    a.out = static_cast<float*>(out);
-    a.status = cache->status;
-    a.cfg = dev_config(c, cache->max_batch);
-    int splits = 1;
-    decode_plan(cache, n, &splits, &a.tiles_per_split);
-    a.splits = splits;
-    if (splits > 1) {
-        const size_t need = decode_ws_bytes(c, n);
-        if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SNAP_ERR_INVALID_ARG;
-        const size_t parts = (size_t)n * c.n_q_heads * MAX_DECODE_SPLITS;
-        a.part_o = static_cast<float*>(ws);
-        a.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + align_up(parts * sizeof(float) * c.d_v, 256));
-    }
-    return cuda_status(run_decode(cache, a, static_cast<cudaStream_t>(stream)));
+    return decode_with_ws(cache, slots, n, q, nullptr, nullptr, out, ws, ws_bytes, stream);
 }
 
 snap_status snap_decode_step(snap_cache* cache, const int32_t* slots, int n, const void* q, const void* k_new,
                              const void* v_new, void* out, void* ws, size_t ws_bytes, void* stream) {
-    snap_status s = snap_decode_append(cache, slots, n, k_new, v_new, stream);
-    return s != SNAP_OK ? s : snap_decode_attn(cache, slots, n, q, out, ws, ws_bytes, stream);
+    if (!k_new) return SNAP_ERR_INVALID_ARG;
+    return decode_with_ws(cache, slots, n, q, k_new, v_new, out, ws, ws_bytes, stream);
 }
 
 snap_status snap_selftest_bounded_wait(snap_cache* cache, void* stream) {
@@ -729,28 +756,15 @@ extern "C" snap_status snap_decode_attn_noalloc(snap_cache* cache, const int32_t
                                                 void* out, void* stream) {
     if (!cache || n < 0) return SNAP_ERR_INVALID_ARG;
     if (n == 0) return SNAP_OK;
-    if (!slots || !q || !out || !aligned16(q) || !aligned16(out)) return SNAP_ERR_INVALID_ARG;
-    if (n > cache->max_batch) return SNAP_ERR_INVALID_ARG;
     const snap_config& c = cache->cfg;
     DecodeArgs a;
-    std::memset(&a, 0, sizeof a);
-    a.kc = cache->k;
-    a.vc = cache->v;
-    a.meta = cache->meta;
-    a.slots = slots;
-    a.n = n;
-    a.q = static_cast<const bf16*>(q);
-    a.out = static_cast<float*>(out);
-    a.status = cache->status;
-    a.cfg = dev_config(c, cache->max_batch);
+    if (const snap_status s = decode_args(cache, slots, n, q, out, nullptr, nullptr, &a); s != SNAP_OK) return s;
     // The scratch address is looked up on every device's first call, whatever its
     // split plan, so that this first call (which may also load the module holding
     // the array) is the one the header tells callers to make before any capture.
     void* scratch = nullptr;
     if (const snap_status s = noalloc_scratch(&scratch); s != SNAP_OK) return s;
-    int splits = 1;
-    decode_plan(cache, n, &splits, &a.tiles_per_split);
-    a.splits = splits;
+    const int splits = a.splits;
     if (splits > 1) {
         // compact partial layout for this call: O then (max, sum)
         const size_t parts = (size_t)n * c.n_q_heads * splits;

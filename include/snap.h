@@ -89,7 +89,8 @@ typedef struct {
     int32_t R0;      /* first prompt position that was written into the ring */
     int32_t n_sink;  /* valid sink slots = min(L_sink, S) */
     int32_t n_mid;   /* valid middle slots = min(K, R0 - n_sink) */
-    int32_t pad[3];
+    int32_t pad[3];  /* library use: pad[0] counts the CTAs of a decode step in flight (zero
+                        between calls) */
 } snap_seq_meta;
 
 /* Device addresses of the regions a cache occupies inside the caller's buffer. */
@@ -124,9 +125,15 @@ snap_status snap_cache_bytes(const snap_config* cfg, int max_batch, size_t* byte
 
 /*
  * Binds a cache to a caller-owned device buffer of at least snap_cache_bytes()
- * bytes (256-byte aligned).  The handle owns host state only; the buffer stays the
- * caller's and must outlive the handle.  Zeroes the whole buffer on `stream`
- * (every slot starts empty).  *out receives the handle.
+ * bytes (256-byte aligned): max_batch static-shape caches of the "Fixed-Size Cache
+ * Layout" section ([L_sink | K | L_recent] slots per KV head, fixed at creation, as the
+ * "Why This Wasn't Already Standard" section asks of static-graph hardware), plus the
+ * per-sequence meta, the selection lists, split-merge counters and the status word.
+ * The handle owns host state only; the buffer stays the caller's and must outlive the
+ * handle.  Zeroes the whole buffer on `stream` (every slot starts empty).  *out
+ * receives the handle.  SNAP_ERR_INVALID_ARG for a null or misaligned buffer, a
+ * buffer smaller than snap_cache_bytes(), or max_batch < 1; SNAP_ERR_CUDA if the
+ * zeroing cannot be queued.
  */
 snap_status snap_cache_create(const snap_config* cfg, int max_batch, void* dev_buf,
                               size_t bytes, void* stream, snap_cache** out);
@@ -213,7 +220,12 @@ snap_status snap_window_logits(snap_cache* cache, const void* K, int64_t S, int6
 snap_status snap_decode_append(snap_cache* cache, const int32_t* slots, int n, const void* k_new,
                                const void* v_new, void* stream);
 
-/* Workspace bytes snap_decode_attn() needs for batches of up to max_n sequences. */
+/*
+ * Workspace bytes snap_decode_attn() needs for batches of up to max_n sequences: the
+ * split-KV partial results (max, sum, un-normalised output) of the "Prefill / Decode
+ * Pipeline" section's memory-bound decode, split over key ranges to fill the GPU.
+ * Host call, no CUDA.  SNAP_ERR_INVALID_ARG for max_n < 1 or a null pointer.
+ */
 snap_status snap_decode_attn_ws_bytes(const snap_config* cfg, int max_n, size_t* bytes);
 
 /*
@@ -230,7 +242,10 @@ snap_status snap_decode_attn_plan(const snap_cache* cache, int n, int* splits, i
 
 /*
  * Split-KV decode attention over the fixed-size cache for a continuous batch whose
- * sequences sit at different ring offsets.  For each b < n and query head i, a plain
+ * sequences sit at different ring offsets ("Prefill / Decode Pipeline": decode is
+ * memory-bound, each step streams the cache once; "Why This Wasn't Already Standard":
+ * requests of one batch sit at different points of their lifecycle; "Fixed-Size Cache
+ * Layout": the attention runs over sinks, selected middle and recent ring).  For each b < n and query head i, a plain
  * softmax over the VALID slots of sequence slots[b] (sinks < n_sink, middle < n_mid,
  * ring slots holding positions max(R0, T - L_recent) .. T-1) of sm_scale * q.k,
  * weighted sum of the values.  The query attends to what the cache holds now: call
@@ -245,9 +260,17 @@ snap_status snap_decode_attn(snap_cache* cache, const int32_t* slots, int n, con
                              void* out, void* ws, size_t ws_bytes, void* stream);
 
 /*
- * One decode step: snap_decode_append() of k_new/v_new followed by snap_decode_attn()
- * of q, on the same stream (the form a serving loop captures into a CUDA graph).
- * Same arguments, results and workspace as the two calls.
+ * One decode step ("Ring Buffer vs. Naive Slicing": each new token is scattered into
+ * its fixed ring slot, then decode attends over the fixed-size cache; "Prefill / Decode
+ * Pipeline": the step streams the cache once): the result of snap_decode_append() of
+ * k_new/v_new followed by snap_decode_attn() of q, with the same arguments and
+ * workspace.  GQA runs it as ONE kernel: the CTA whose key range holds the new token's
+ * ring slot writes the row before reading, every CTA attends over T + 1 tokens, the
+ * last CTA of each sequence advances T and the last CTA of each (sequence, KV head)
+ * merges the key splits.  MLA runs the attention kernel (with the same fused append)
+ * and, when the plan splits the keys, the merge kernel.  Static shapes and no host
+ * synchronisation: the form a serving loop captures into a CUDA graph.
+ * SNAP_ERR_INVALID_ARG for a null k_new (and, for GQA, a null v_new).
  */
 snap_status snap_decode_step(snap_cache* cache, const int32_t* slots, int n, const void* q, const void* k_new,
                              const void* v_new, void* out, void* ws, size_t ws_bytes, void* stream);

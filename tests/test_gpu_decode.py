@@ -87,8 +87,9 @@ def test_decode_continuous_batch_ring_offsets():
 
 
 def test_fused_decode_step_continuous_batch():
-    """snap_decode_step (append, then attention, on one stream) over a continuous batch at
-    different ring offsets, with splits (cache 4096) and without (cache 128)."""
+    """snap_decode_step (for GQA one kernel: ring append, attention, split merge) over a
+    continuous batch at different ring offsets, with splits (cache 4096) and without
+    (cache 128); every output against the oracle and the ring bit-exact afterwards."""
     for C_parts, lengths in (((4, 2044, 2048), [6000, 300, 2100, 4500]), ((4, 60, 64), [300, 37, 129, 2])):
         wl = inputs.Workload("fused", 0, 32, 8, 128, 128, *C_parts, 16, 7, 4, 0, 0, 0, 1 / math.sqrt(128))
         b = Batch(wl, lengths, slots=[2, 0, 3, 1], seed=17, max_batch=4)
@@ -259,3 +260,46 @@ def test_compress_on_second_stream_while_decoding():
             oracle.append(ocs[i], tok.k[i], tok.v[i])
             check_outputs(out[i], oracle.decode_attn(ocs[i], tok.q[i]), f"joined, step {t} seq {i}")
     assert b.cache.check_device() == snap.SNAP_OK
+
+
+def test_fused_decode_step_mla():
+    """The MLA layout's snap_decode_step (append fused into the attention kernel, merge
+    kernel after) over a ragged cache whose ring wraps, against the oracle."""
+    wl = inputs.Workload("mla_fused", 1, 128, 1, 576, 512, 4, 40, 100, 4, 5, 1, 0, 0, 0,
+                         1 / math.sqrt(192))
+    b = Batch(wl, [700, 90, 260], [2, 0, 1], seed=15, max_batch=3)
+    for t in range(105):
+        b.step(t, fused=True)
+    b.check_rows()
+
+
+def _kernels_of(fn):
+    """Names of the GPU kernels one call launches (torch profiler)."""
+    from torch.profiler import ProfilerActivity, profile
+    torch.cuda.synchronize()
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        fn()
+        torch.cuda.synchronize()
+    names = []
+    for e in prof.events():
+        dt = str(getattr(e, "device_type", ""))
+        if "CUDA" in dt and ("kernel" in e.name or "decode" in e.name or "append" in e.name):
+            names.append(e.name)
+    return names
+
+
+@pytest.mark.parametrize("C_parts,lengths", [((4, 2044, 2048), [6000, 300, 2100, 4500]),
+                                             ((4, 16380, 16384), [20000, 9000])])
+def test_gqa_decode_step_is_one_launch(C_parts, lengths):
+    """A GQA decode step is one kernel launch whatever the split plan (the ring append
+    and the split merge run inside the attention kernel)."""
+    wl = inputs.Workload("one", 0, 32, 8, 128, 128, *C_parts, 16, 7, len(lengths), 0, 0, 0, 1 / math.sqrt(128))
+    b = Batch(wl, lengths, slots=list(range(len(lengths))), seed=19)
+    splits = b.cache.decode_attn_plan(len(lengths))[0]
+    tok = inputs.gen_decode(wl, len(lengths), step=0, seed=19)
+    q, k, v = tok.q.cuda(), tok.k.cuda(), tok.v.cuda()
+    b.cache.decode_step(b.dslots, q, k, v)         # first call: one-time set-up outside the profile
+    names = _kernels_of(lambda: b.cache.decode_step(b.dslots, q, k, v))
+    if not names:
+        pytest.skip("the profiler reported no kernels on this box")
+    assert names == ["gqa_decode_kernel"] or (len(names) == 1 and "gqa_decode_kernel" in names[0]), (splits, names)
