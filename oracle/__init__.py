@@ -95,6 +95,7 @@ def _load():
             lib.snap_oracle_slot_position.restype = i64
             lib.snap_oracle_append.argtypes = [P(_Config), vp, vp, P(_Meta), vp, vp]
             lib.snap_oracle_decode_attn.argtypes = [P(_Config), vp, vp, P(_Meta), vp, vp]
+            lib.snap_oracle_prefill_attn.argtypes = [P(_Config), i64, vp, vp, vp, i64, i64, vp, vp]
             _lib = lib
     return _lib
 
@@ -311,3 +312,17 @@ def decode_attn(cache: Cache, q) -> np.ndarray:
     if rc != 0:
         raise ValueError(f"oracle decode_attn rc={rc}")
     return out
+
+
+def prefill_attn(cfg: Config, Q, K, V):
+    """Causal prefill attention: Q [S][H_q][d], K/V [S][H_kv][d] bf16 ->
+    (out [S][H_q][d_v] float64, lse [S][H_q] float64, natural log)."""
+    qb, kb, vb = _bits(Q), _bits(K), _bits(V)
+    S = qb.shape[0]
+    out = np.zeros((S, cfg.n_q_heads, cfg.d_v), np.float64)
+    lse = np.zeros((S, cfg.n_q_heads), np.float64)
+    rc = _load().snap_oracle_prefill_attn(ctypes.byref(cfg._c()), S, _ptr(qb), _ptr(kb), _ptr(vb),
+                                          cfg.n_kv_heads * cfg.d_qk, cfg.d_qk, _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle prefill_attn rc={rc}")
+    return out, lse

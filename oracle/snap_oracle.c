@@ -366,3 +366,45 @@ int snap_oracle_decode_attn(const snap_oracle_config* c, const uint16_t* cache_k
     free(s);
     return 0;
 }
+
+int snap_oracle_prefill_attn(const snap_oracle_config* c, int64_t S, const uint16_t* Q,
+                             const uint16_t* Kp, const uint16_t* Vp,
+                             int64_t k_tok_stride, int64_t k_head_stride,
+                             double* out, double* lse)
+{
+    if (snap_oracle_check_config(c) != 0 || c->layout != 0 || S < 1 || !Q || !Kp || !Vp) return -1;
+    const int G = c->n_q_heads / c->n_kv_heads;
+    const int dk = c->d_qk, dv = c->d_v;
+    double* s = (double*)malloc(sizeof(double) * (size_t)S);
+    if (!s) return -3;
+    for (int64_t i = 0; i < S; ++i) {
+        for (int hq = 0; hq < c->n_q_heads; ++hq) {
+            const int h = hq / G;
+            const uint16_t* q = Q + (i * c->n_q_heads + hq) * (int64_t)dk;
+            /* scores of the causal row: keys 0..i */
+            const int64_t last = i - (ORACLE_MUTANT == 9 && i > 0);
+            double mx = -INFINITY;
+            for (int64_t j = 0; j <= last; ++j) {
+                const uint16_t* k = Kp + j * k_tok_stride + (int64_t)h * k_head_stride;
+                double dot = 0.0;
+                for (int e = 0; e < dk; ++e) dot += bf16_value(q[e]) * bf16_value(k[e]);
+                s[j] = c->sm_scale * dot;
+                if (s[j] > mx) mx = s[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j <= last; ++j) l += exp(s[j] - mx);
+            if (lse) lse[i * c->n_q_heads + hq] = mx + log(l);
+            if (out) {
+                double* o = out + (i * c->n_q_heads + hq) * (int64_t)dv;
+                for (int e = 0; e < dv; ++e) o[e] = 0.0;
+                for (int64_t j = 0; j <= last; ++j) {
+                    const double p = exp(s[j] - mx) / l;
+                    const uint16_t* v = Vp + j * k_tok_stride + (int64_t)h * k_head_stride;
+                    for (int e = 0; e < dv; ++e) o[e] += p * bf16_value(v[e]);
+                }
+            }
+        }
+    }
+    free(s);
+    return 0;
+}

@@ -19,6 +19,9 @@
  * top-K selection", Infinity-Bench section of the same page), and the K best
  * middle positions are kept (ties: lower position wins), stored ascending.
  *
+ * It also holds plain causal prefill attention (with the per-row log-sum-exp that a
+ * prefill flash-attention kernel hands to the compression).
+ *
  * Arithmetic: every input is a bf16 bit pattern (uint16_t); all arithmetic is
  * IEEE double.  Readings of points the pages leave open are listed beside each
  * function.  Parity pins live in tests/test_oracle_pins.py.
@@ -123,6 +126,21 @@ int snap_oracle_compress_scored(const snap_oracle_config* c, int64_t S,
                                 const double* col,
                                 uint16_t* cache_k, uint16_t* cache_v,
                                 int32_t* sel, double* pool, snap_oracle_meta* m);
+
+/*
+ * Causal prefill attention of one prompt (the prefill that precedes compression; the
+ * episode companion page's headline figure puts compression at 2-5% extra prefill
+ * latency).  Plain definition, every query against every key up to its own position:
+ *   Q:   [S][H_q][d_qk];  Kp/Vp: keys / values with the strides of snap_oracle_compress
+ *   out: [S][H_q][d_v]  softmax(sm_scale * q.k) weighted sum of the values (double)
+ *   lse: [S][H_q]       natural log of sum_j exp(sm_scale * q.k_j) over the causal row,
+ *                       the quantity a flash-attention kernel keeps per query row
+ * GQA only (query head i reads KV head i / G).  Either output may be NULL.
+ */
+int snap_oracle_prefill_attn(const snap_oracle_config* c, int64_t S, const uint16_t* Q,
+                             const uint16_t* Kp, const uint16_t* Vp,
+                             int64_t k_tok_stride, int64_t k_head_stride,
+                             double* out, double* lse);
 
 /* Ring slot (within the whole cache) that holds absolute position p. */
 int64_t snap_oracle_ring_slot(const snap_oracle_config* c, int64_t p);

@@ -1,8 +1,8 @@
 """The pins catch plausible mistakes: each mutant build of the oracle carries one
 deliberate error (a dropped scale, an off-by-one causal limit, a wrong head
 grouping, a wrong pooling radius, reversed tie-breaking, a wrong ring slot, invalid
-middle slots treated as valid, a transposed value row), and the pin suite run
-against it must fail.  CPU only."""
+middle slots treated as valid, a transposed value row, a prefill row missing its
+diagonal key), and the pin suite run against it must fail.  CPU only."""
 import os
 import subprocess
 import sys
@@ -21,6 +21,7 @@ MUTANTS = {
     6: "ring slot missing the L_sink + K offset",
     7: "unused middle slots treated as valid",
     8: "value row read backwards",
+    9: "prefill attention row stops before the query's own key",
 }
 
 

@@ -371,3 +371,51 @@ def test_mla_attention_is_mqa_with_latent_values(oracle_lib):
     kf = K.double()[:, 0, :].unsqueeze(0).expand(16, S, 24)
     ref = _sdpa(q.double(), kf, kf[..., :16], 0.3)
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+
+
+# -------------------------------------------------------------------- prefill attention
+
+def test_prefill_attention_equals_causal_sdpa(oracle_lib):
+    """Causal prefill attention with grouped KV heads equals torch SDPA (float64,
+    is_causal) over the same rows, and its log-sum-exp equals torch.logsumexp of the
+    scaled, causally masked scores."""
+    c = cfg_of(Hq=8, Hkv=2, dk=16, dv=16)
+    S = 37
+    Q, K, V = bf16((S, 8, 16), 51), bf16((S, 2, 16), 52), bf16((S, 2, 16), 53)
+    out, lse = oracle.prefill_attn(c, Q, K, V)
+    q = Q.double().permute(1, 0, 2)                                   # [H][S][d]
+    k = K.double().permute(1, 0, 2).repeat_interleave(4, dim=0)
+    v = V.double().permute(1, 0, 2).repeat_interleave(4, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True, scale=c.sm_scale)
+    np.testing.assert_allclose(out, ref.permute(1, 0, 2).numpy(), rtol=1e-12, atol=1e-13)
+    s = c.sm_scale * (q @ k.transpose(1, 2))
+    s = s.masked_fill(torch.ones(S, S, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=2).T.numpy(), rtol=1e-13, atol=1e-13)
+
+
+def test_prefill_lse_of_window_rows_equals_window_scores_lse(oracle_lib):
+    """The last W rows' prefill log-sum-exp is the window scoring's row normaliser (two
+    separate loops of the oracle): the quantity snap_compress_lse takes from a prefill."""
+    c = cfg_of(Hq=8, Hkv=2, dk=16, dv=16, W=5)
+    S = 41
+    Q, K, V = bf16((S, 8, 16), 54), bf16((S, 2, 16), 55), bf16((S, 2, 16), 56)
+    _, lse = oracle.prefill_attn(c, Q, K, V)
+    lse_w, _ = oracle.window_scores(c, K, Q[S - c.W:].contiguous())       # [H_kv][W][G]
+    for w in range(c.W):
+        for hq in range(8):
+            assert abs(lse[S - c.W + w, hq] - lse_w[hq // 4, w, hq % 4]) <= 1e-13 * max(1.0, abs(lse_w[hq // 4, w, hq % 4]))
+
+
+def test_prefill_zero_keys_closed_form(oracle_lib):
+    """With all-zero keys every causal row is uniform: row i averages values 0..i and its
+    log-sum-exp is log(i + 1)."""
+    c = cfg_of(Hq=4, Hkv=1, dk=8, dv=8)
+    S = 19
+    Q, V = bf16((S, 4, 8), 57), bf16((S, 1, 8), 58)
+    K = torch.zeros((S, 1, 8), dtype=torch.bfloat16)
+    out, lse = oracle.prefill_attn(c, Q, K, V)
+    vd = V.double()[:, 0]
+    for i in range(S):
+        np.testing.assert_allclose(out[i], vd[:i + 1].mean(dim=0).numpy()[None].repeat(4, 0), rtol=1e-13,
+                                   atol=1e-14)
+        np.testing.assert_allclose(lse[i], np.full(4, math.log(i + 1)), rtol=1e-14, atol=1e-14)
