@@ -151,4 +151,17 @@ cudaError_t launch_score_tc(int mode, const CUtensorMap& tx, const CUtensorMap& 
                             int D, bool x_is_q, bool x_resident, int num_sms, cudaStream_t st);
 cudaError_t launch_cache_write(const CompressArgs& a, int num_sms, cudaStream_t st);
 
+// ------------------------------------------- causal prefill attention (tcgen05 + TMA)
+struct PrefillArgs {
+    int S, Hq, G, W;
+    float sl2;                   // sm_scale * log2(e)
+    bf16* O;                     // [S][Hq][128] output
+    int64_t o_tok_stride;        // elements
+    float* lse_obs;              // [W][Hq] natural-log LSE of the last W rows (nullable)
+    int32_t* status;
+};
+// tq: Q {128, S, Hq}, tk / tv: K / V {128, S, Hkv}; boxes {64, 128, 1}, 128-byte swizzle
+cudaError_t launch_prefill_tc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const PrefillArgs& a, cudaStream_t st);
+
 }  // namespace snap

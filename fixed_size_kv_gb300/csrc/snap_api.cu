@@ -642,6 +642,39 @@ snap_status snap_window_logits(snap_cache* cache, const void* K, int64_t S, int6
                                    static_cast<cudaStream_t>(stream)));
 }
 
+snap_status snap_prefill_attn(snap_cache* cache, const void* Q, int64_t S, const void* K, const void* V,
+                              int64_t tok_stride, int64_t head_stride, void* O, float* lse_obs, void* stream) {
+    if (!cache || !Q || !K || !V || !O) return SNAP_ERR_INVALID_ARG;
+    const snap_config& c = cache->cfg;
+    if (c.layout != SNAP_LAYOUT_GQA) return SNAP_ERR_UNSUPPORTED;
+    if (S < 1 || S > (1ll << 30)) return SNAP_ERR_SHAPE;
+    if (lse_obs && S < c.W) return SNAP_ERR_SHAPE;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return SNAP_ERR_INVALID_ARG;
+    if (lse_obs && (reinterpret_cast<uintptr_t>(lse_obs) & 3u)) return SNAP_ERR_INVALID_ARG;
+    if (tok_stride < c.d_qk || (tok_stride * 2) % 16 || head_stride < 0 || (head_stride * 2) % 16)
+        return SNAP_ERR_INVALID_ARG;
+    if (c.n_kv_heads > 1 && head_stride < c.d_qk) return SNAP_ERR_INVALID_ARG;
+    if (num_sms() <= 0) return SNAP_ERR_CUDA;
+    CUtensorMap tq, tk, tv;
+    const cuuint64_t qd[3] = {(cuuint64_t)c.d_qk, (cuuint64_t)S, (cuuint64_t)c.n_q_heads};
+    const cuuint64_t qs[2] = {(cuuint64_t)c.n_q_heads * c.d_qk * 2, (cuuint64_t)c.d_qk * 2};
+    const cuuint32_t qb[3] = {64, 128, 1};
+    if (!encode(&tq, Q, 3, qd, qs, qb) || !k_map(&tk, K, S, c, tok_stride, head_stride, 128) ||
+        !k_map(&tv, V, S, c, tok_stride, head_stride, 128))
+        return SNAP_ERR_INVALID_ARG;
+    PrefillArgs a;
+    a.S = (int)S;
+    a.Hq = c.n_q_heads;
+    a.G = c.n_q_heads / c.n_kv_heads;
+    a.W = c.W;
+    a.sl2 = c.sm_scale * 1.4426950408889634f;
+    a.O = static_cast<bf16*>(O);
+    a.o_tok_stride = (int64_t)c.n_q_heads * c.d_qk;
+    a.lse_obs = lse_obs;
+    a.status = cache->status;
+    return cuda_status(launch_prefill_tc(tq, tk, tv, a, static_cast<cudaStream_t>(stream)));
+}
+
 snap_status snap_decode_append(snap_cache* cache, const int32_t* slots, int n, const void* k_new,
                                const void* v_new, void* stream) {
     if (!cache || n < 0) return SNAP_ERR_INVALID_ARG;

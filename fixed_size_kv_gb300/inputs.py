@@ -153,6 +153,18 @@ def gen_prefill(wl: Workload, S: int, seed: int, seq: int = 0, device="cpu",
     return Prefill(K=K.to(torch.bfloat16), V=V, Q=Q, heavy=heavy)
 
 
+def gen_prompt_queries(wl: Workload, pre: Prefill, seed: int, seq: int = 0, device="cpu") -> torch.Tensor:
+    """Queries of every prompt position, bf16 [S][H_q][d_qk], for the prefill attention:
+    fresh N(0,1) rows for positions 0 .. S-W-1 and the prefill's observation-window
+    queries (pre.Q) for the last W positions."""
+    S = pre.K.shape[0]
+    g = _gen(seed, 307, seq, device=device)
+    Q = _randn((S, wl.n_q_heads, wl.d_qk), g, device).to(torch.bfloat16)
+    W = min(wl.W, S)
+    Q[S - W:] = pre.Q[wl.W - W:].to(device)
+    return Q
+
+
 @dataclass
 class DecodeToken:
     q: torch.Tensor            # bf16 [n][H_q][d_qk]

@@ -68,6 +68,7 @@ SIGNATURES = {
     "snap_compress_stages": (_I, [_VP, _I, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _SZ, _I, _VP]),
     "snap_window_logits": (_I, [_VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP]),
     "snap_decode_append": (_I, [_VP, _VP, _I, _VP, _VP, _VP]),
+    "snap_prefill_attn": (_I, [_VP, _VP, _I64, _VP, _VP, _I64, _I64, _VP, _VP, _VP]),
     "snap_decode_attn_ws_bytes": (_I, [_P(snap_config), _I, _P(_SZ)]),
     "snap_decode_attn_plan": (_I, [_VP, _I, _P(_I), _P(_I), _P(_I)]),
     "snap_selftest_bounded_wait": (_I, [_VP, _VP]),
@@ -252,6 +253,23 @@ class SnapCache:
         _check(load().snap_window_logits(self.handle, _ptr(K), S, K.stride(0), K.stride(1), _ptr(Q_obs),
                                          _ptr(out), _stream(stream)), "snap_window_logits")
         return out
+
+    def prefill_attn(self, Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, O: torch.Tensor | None = None,
+                     lse_obs: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """snap_prefill_attn: causal attention of one prompt (Q [S][H_q][128] contiguous,
+        K/V [S][H_kv][128] with unit inner stride); writes O (bf16, same shape as Q) and,
+        if given, lse_obs fp32 [W][H_q] for the last W rows.  Returns O."""
+        S = Q.shape[0]
+        Q = Q.contiguous()
+        assert K.stride(2) == 1 and V.stride() == K.stride()
+        if O is None:
+            O = torch.empty_like(Q)
+        assert O.is_contiguous() and O.dtype == torch.bfloat16
+        if lse_obs is not None:
+            assert lse_obs.dtype == torch.float32 and lse_obs.is_contiguous()
+        _check(load().snap_prefill_attn(self.handle, _ptr(Q), S, _ptr(K), _ptr(V), K.stride(0), K.stride(1),
+                                        _ptr(O), _ptr(lse_obs), _stream(stream)), "snap_prefill_attn")
+        return O
 
     def decode_append(self, slots: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor | None,
                       stream=None) -> None:

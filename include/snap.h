@@ -211,6 +211,25 @@ snap_status snap_window_logits(snap_cache* cache, const void* K, int64_t S, int6
                                int64_t head_stride, const void* Q_obs, float* out, void* stream);
 
 /*
+ * Causal prefill attention of one prompt, GQA layout (head_dim 128), on the tensor
+ * cores: O[i][h] = softmax_j<=i(sm_scale * q_{i,h} . k_{j,h/G}) v_{j,h/G}, plus the
+ * log-sum-exp of the last W rows in the layout snap_compress_lse() takes.  The episode
+ * companion page's headline figure puts the compression at "2-5% extra prefill
+ * latency": a prefill that already holds each query row's log-sum-exp hands it over,
+ * and the compression skips its own row pass.
+ *  Q        bf16 [S][n_q_heads][128], contiguous
+ *  K, V     bf16 keys / values with element (j, h, e) at base + j*tok_stride +
+ *           h*head_stride + e (the strides of snap_compress)
+ *  O        bf16 [S][n_q_heads][128] output (contiguous)
+ *  lse_obs  fp32 [W][n_q_heads] (nullable): natural-log LSE of rows S-W .. S-1
+ * The cache handle supplies the configuration (heads, W, sm_scale) and the status word
+ * only.  SNAP_ERR_UNSUPPORTED for the MLA layout; SNAP_ERR_SHAPE for S < 1 or, with
+ * lse_obs, S < W; SNAP_ERR_INVALID_ARG for null or misaligned pointers or strides.
+ */
+snap_status snap_prefill_attn(snap_cache* cache, const void* Q, int64_t S, const void* K, const void* V,
+                              int64_t tok_stride, int64_t head_stride, void* O, float* lse_obs, void* stream);
+
+/*
  * Decode-step append for a continuous batch ("Ring Buffer vs. Naive Slicing"): for each
  * b < n, the new token of sequence slots[b] (position T) is written into ring slot
  * L_sink + K + (T mod L_recent), then T += 1.  No gather, no concat.
