@@ -54,6 +54,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-full-kv", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-prefill", action="store_true",
+                   help="skip the prefill-attention timing (compression as prefill overhead)")
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the short runs of the other four workloads that the 128k line carries")
     p.add_argument("--capacity", type=float, default=0.0, metavar="GIB",
@@ -427,9 +429,36 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
         del fcache, fgraph
         torch.cuda.empty_cache()
 
+    # ---------------------------------------------------------------- prefill attention of the first
+    # prompt (GQA): its time, its tensor roofline, and the compression as overhead on it
+    prefill = None
+    lse0 = None
+    if wl.layout == 0 and not args.no_prefill:
+        from fixed_size_kv_gb300 import inputs
+        p0 = pre[0]
+        S0 = p0.K.shape[0]
+        with torch.cuda.stream(stream):
+            Qf = inputs.gen_prompt_queries(wl, p0, seed=replica_seed(args.seed, rank), seq=0, device=dev)
+            Of = torch.empty_like(Qf)
+            lse0 = torch.empty((wl.W, wl.n_q_heads), dtype=torch.float32, device=dev)
+        pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+        for e0_, e1_ in pe:
+            e0_.record(stream)
+            cache.prefill_attn(Qf, p0.K, p0.V, O=Of, lse_obs=lse0, stream=stream)
+            e1_.record(stream)
+        stream.synchronize()
+        pre_ms = min(a_.elapsed_time(b_) for a_, b_ in pe[1:])
+        pflop = 2.0 * wl.n_q_heads * wl.d_qk * S0 * (S0 + 1)      # QK^T and PV over the causal half
+        prefill = {"prompt_len": S0, "ms": pre_ms, "flop": pflop,
+                   "achieved_tflops": pflop / (pre_ms / 1e3) / 1e12,
+                   "frac": pflop / (pre_ms / 1e3) / 1e12 / bf16_burst, "peak": bf16_burst,
+                   "peak_kind": "bf16 burst", "kernel": "prefill_tc_kernel (snap_prefill_attn)"}
+        del Qf, Of
     # ---------------------------------------------------------------- compression, stage by stage,
     # and with the prefill's log-sum-exp supplied (snap_compress_lse: no row pass)
     lses = [window_lse(wl, p.K, p.Q) for p in pre]
+    if lse0 is not None:
+        lses[0] = lse0              # the prefill kernel's own log-sum-exp for the first prompt
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for rep in range(2):
@@ -440,6 +469,21 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
         stream.synchronize()
     cmp_lse_ms = e0.elapsed_time(e1) / B
     stage_ms = time_compress_stages(cache, pre, stream)
+    if prefill is not None:
+        e0.record(stream)
+        cache.compress_lse(0, pre[0].K, pre[0].V, pre[0].Q, lses[0], stream=stream)
+        e1.record(stream)
+        stream.synchronize()
+        c_lse0 = e0.elapsed_time(e1)
+        e0.record(stream)
+        cache.compress(0, pre[0].K, pre[0].V, pre[0].Q, stream=stream)
+        e1.record(stream)
+        stream.synchronize()
+        c_full0 = e0.elapsed_time(e1)
+        prefill["compress_with_prefill_lse_ms"] = c_lse0
+        prefill["compress_both_passes_ms"] = c_full0
+        prefill["overhead_frac"] = c_lse0 / prefill["ms"]
+        prefill["overhead_frac_both_passes"] = c_full0 / prefill["ms"]
     del lses
     F = score_pass_flop(wl, lengths)
     tf = lambda ms: F / (ms / 1e3) / 1e12 if ms else None  # noqa: E731
@@ -497,6 +541,8 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
                          "frac": attn_gbs / hbm_peak, "peak_source": peak_kind,
                          "traffic": traffic_record(wl.name)},
             "compress_roofline": compress_roofline,
+            "prefill": prefill,
+            "prefill_overhead_frac": prefill["overhead_frac"] if prefill else None,
             "gpu_launches": per_step_launches * steps,
         },
     }

@@ -46,50 +46,75 @@ __global__ void append_kernel(AppendArgs a) {
 
 // Prefill cache build: every slot of the sequence is written, with the row of
 // the position it holds, or zeros when it holds nothing (so a reused cache slot
-// never carries a previous request's rows).
-__global__ void cache_write_kernel(CompressArgs a) {
+// never carries a previous request's rows).  One warp per cache row (KV head h,
+// slot s), four rows in flight per warp: the lanes copy the row's 16-byte chunks (a GQA
+// row is 16 K chunks + 16 V chunks, one per lane; an MLA row 72 key chunks).
+constexpr int CW_ROWS = 4;
+
+__device__ __forceinline__ int cache_row_position(const CompressArgs& a, const int32_t* sel_h, int s) {
     const DevConfig& c = a.cfg;
-    const int h = blockIdx.y;
-    const int ck = c.dqk / 8, cv = (c.layout == SNAP_LAYOUT_GQA) ? c.dv / 8 : 0;
-    const int per_slot = ck + cv;
-    const int32_t* sel_h = a.sel + ((size_t)a.slot * c.Hkv + h) * c.K;
     const int ring0 = c.L_sink + c.K;
-    const int R0m = a.R0 % c.L_recent;
-    const size_t total = (size_t)c.C * per_slot;
-    for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-         idx += (size_t)gridDim.x * blockDim.x) {
-        const int s = (int)(idx / per_slot), ch = (int)(idx % per_slot);
-        int p = -1;
-        if (s < c.L_sink) {
-            p = s < a.n_sink ? s : -1;
-        } else if (s < ring0) {
-            const int i = s - c.L_sink;
-            if (i < a.n_mid) p = a.scored ? sel_h[i] : c.L_sink + i;
-        } else {
-            int off = (s - ring0) - R0m;
-            if (off < 0) off += c.L_recent;
-            const int q = a.R0 + off;  // the position congruent to this ring slot in [R0, R0+L_recent)
-            p = q < a.S ? q : -1;
+    if (s < c.L_sink) return s < a.n_sink ? s : -1;
+    if (s < ring0) {
+        const int i = s - c.L_sink;
+        if (i >= a.n_mid) return -1;
+        return a.scored ? __ldg(sel_h + i) : c.L_sink + i;
+    }
+    int off = (s - ring0) - a.R0 % c.L_recent;
+    if (off < 0) off += c.L_recent;
+    const int q = a.R0 + off;   // the position congruent to this ring slot in [R0, R0 + L_recent)
+    return q < a.S ? q : -1;
+}
+
+__global__ void __launch_bounds__(256) cache_write_kernel(CompressArgs a) {
+    const DevConfig& c = a.cfg;
+    const int lane = threadIdx.x & 31;
+    const int ck = c.dqk / 8, cv = (c.layout == SNAP_LAYOUT_GQA) ? c.dv / 8 : 0;
+    const int per_row = ck + cv;
+    const int64_t rows = (int64_t)c.Hkv * c.C;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t w0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    for (int64_t r0 = w0 * CW_ROWS; r0 < rows; r0 += warps * CW_ROWS) {
+        int pos[CW_ROWS];
+#pragma unroll
+        for (int u = 0; u < CW_ROWS; ++u) {
+            const int64_t r = r0 + u;
+            pos[u] = -1;
+            if (r < rows) {
+                const int h = (int)(r / c.C), s = (int)(r % c.C);
+                pos[u] = cache_row_position(a, a.sel + ((size_t)a.slot * c.Hkv + h) * c.K, s);
+            }
         }
-        const size_t row = ((size_t)a.slot * c.Hkv + h) * (size_t)c.C + s;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (ch < ck) {
-            if (p >= 0)
-                v = reinterpret_cast<const uint4*>(a.K + (size_t)p * a.tok_stride + (size_t)h * a.head_stride)[ch];
-            reinterpret_cast<uint4*>(a.kc + row * c.dqk)[ch] = v;
-        } else {
-            const int cc = ch - ck;
-            if (p >= 0)
-                v = reinterpret_cast<const uint4*>(a.V + (size_t)p * a.tok_stride + (size_t)h * a.head_stride)[cc];
-            reinterpret_cast<uint4*>(a.vc + row * c.dv)[cc] = v;
+        for (int ch = lane; ch < per_row; ch += 32) {
+            uint4 v[CW_ROWS];
+#pragma unroll
+            for (int u = 0; u < CW_ROWS; ++u) {
+                const int64_t r = r0 + u;
+                v[u] = make_uint4(0u, 0u, 0u, 0u);
+                if (r < rows && pos[u] >= 0) {
+                    const int h = (int)(r / c.C);
+                    const size_t src = (size_t)pos[u] * a.tok_stride + (size_t)h * a.head_stride;
+                    v[u] = ch < ck ? __ldg(reinterpret_cast<const uint4*>(a.K + src) + ch)
+                                   : __ldg(reinterpret_cast<const uint4*>(a.V + src) + (ch - ck));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < CW_ROWS; ++u) {
+                const int64_t r = r0 + u;
+                if (r >= rows) continue;
+                const size_t row = (size_t)a.slot * rows + r;      // [slot][h][s]
+                if (ch < ck) reinterpret_cast<uint4*>(a.kc + row * c.dqk)[ch] = v[u];
+                else reinterpret_cast<uint4*>(a.vc + row * c.dv)[ch - ck] = v[u];
+            }
         }
     }
     // selected-position list for sequences that needed no scoring
-    if (!a.scored && blockIdx.x == 0) {
+    if (!a.scored && blockIdx.x < c.Hkv) {
+        const int h = blockIdx.x;
         int32_t* out = a.sel + ((size_t)a.slot * c.Hkv + h) * c.K;
         for (int i = threadIdx.x; i < c.K; i += blockDim.x) out[i] = i < a.n_mid ? c.L_sink + i : -1;
     }
-    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
         snap_seq_meta m;
         m.S = a.S;
         m.T = a.S;
@@ -109,14 +134,13 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_cache_write(const CompressArgs& a, int num_sms, cudaStream_t st) {
-    const int per_slot = a.cfg.dqk / 8 + (a.cfg.layout == SNAP_LAYOUT_GQA ? a.cfg.dv / 8 : 0);
-    const long long total = (long long)a.cfg.C * per_slot;
-    long long want = (total + 255) / 256;
-    int bx = (int)(want < 1 ? 1 : want);
-    const int cap = (num_sms * 8 + a.cfg.Hkv - 1) / a.cfg.Hkv;
-    if (bx > cap) bx = cap;
-    dim3 grid(bx, a.cfg.Hkv);
-    cache_write_kernel<<<grid, 256, 0, st>>>(a);
+    // one wave of 8 CTAs (64 warps) per SM, fewer when the cache has fewer row groups
+    const long long groups = ((long long)a.cfg.Hkv * a.cfg.C + CW_ROWS - 1) / CW_ROWS;
+    long long blocks = (groups + 7) / 8;
+    const long long cap = (long long)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < a.cfg.Hkv) blocks = a.cfg.Hkv;       // the unscored selection list: one CTA per head
+    cache_write_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 
