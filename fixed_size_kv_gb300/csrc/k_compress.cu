@@ -46,11 +46,14 @@ __global__ void lse_merge_kernel(CompressArgs a) {
 
 // ------------------------------------------------------------------- select
 // One cluster of SEL_CLUSTER CTAs per KV head; CTA r owns a contiguous slice of
-// the middle positions.  Pooled scores (non-negative floats, compared as their
-// IEEE bit patterns, which order them) are written once; the K-th largest is
-// found by a 4 x 8-bit radix descent whose per-CTA histograms are summed through
-// distributed shared memory; an ordered compaction then keeps every score above
-// it and, among the scores equal to it, the lowest positions.
+// the middle positions.  The slice's column sums (plus the pooling halo) are read
+// once into shared memory and max-pooled there; the pooled scores (non-negative
+// floats, compared as their IEEE bit patterns, which order them) stay in shared
+// memory for the rest of the kernel (the workspace takes them when a slice is too
+// long).  The K-th largest is found by a 4 x 8-bit radix descent whose per-CTA
+// histograms are summed through distributed shared memory, the digit of each pass
+// picked by one warp's scan; an ordered compaction then keeps every score above it
+// and, among the scores equal to it, the lowest positions.
 constexpr int SEL_THREADS = 1024;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
 constexpr int SEL_CLUSTER = 8;
@@ -84,12 +87,42 @@ __device__ __forceinline__ int block_excl_scan(int x, int* warp_tot, int* total)
     return r;
 }
 
+// Digit of this radix pass that holds the kk-th largest value: the largest d with
+// (count of digits > d) < kk <= (count of digits >= d).  Warp 0; lane l scans digits
+// 255 - 8l .. 248 - 8l after an exclusive scan of the lanes' totals.
+__device__ __forceinline__ void find_digit(const int* hist, int kk, int* digit, int* kk_left) {
+    const int lane = threadIdx.x & 31;
+    int v[8], tot = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        v[e] = hist[255 - (8 * lane + e)];
+        tot += v[e];
+    }
+    int incl = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int cum = incl - tot;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        if (cum < kk && cum + v[e] >= kk) {
+            *digit = 255 - (8 * lane + e);
+            *kk_left = kk - cum;
+        }
+        cum += v[e];
+    }
+}
+
 __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 1)
-    select_kernel(CompressArgs a) {
+    select_kernel(CompressArgs a, int in_smem) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
+    extern __shared__ uint32_t sel_dyn[];         // [per] pooled bits, then [per + 2 rad] raw sums
     __shared__ int hist_w[SEL_WARPS][256];       // per-warp private histograms
     __shared__ int hist_cta[2][256];             // this CTA's histogram, double-buffered by pass
+    __shared__ int hist_all[256];
     __shared__ int warp_tot[33];
     __shared__ int counts[2];                    // this CTA's (greater, equal) counts
     __shared__ uint32_t sh_prefix;
@@ -105,15 +138,34 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
     const int i0 = min(M, rank * per), i1 = min(M, i0 + per);
     const float* c0 = a.col + (size_t)h * a.S_pad;
     const float* c1 = a.col + ((size_t)c.Hkv + h) * a.S_pad;
-    uint32_t* pool = a.pool + (size_t)h * a.S_pad;
+    // this CTA's pooled values: shared memory when they fit, else the workspace
+    uint32_t* vals = in_smem ? sel_dyn - i0 : a.pool + (size_t)h * a.S_pad;
 
     // 0. pooled scores of this slice (the score GEMM leaves each column sum in two halves)
-    for (int i = i0 + tid; i < i1; i += SEL_THREADS) {
-        const int j = c.L_sink + i;
-        const int lo = max(0, j - rad), hi = min(n_sc - 1, j + rad);
-        float mx = c0[lo] + c1[lo];
-        for (int k = lo + 1; k <= hi; ++k) mx = fmaxf(mx, c0[k] + c1[k]);
-        pool[i] = __float_as_uint(mx);
+    if (in_smem) {
+        // the column sums of positions L_sink + i0 - rad .. L_sink + i1 - 1 + rad, once
+        float* raw = reinterpret_cast<float*>(sel_dyn + per);
+        const int k0 = c.L_sink + i0 - rad;
+        const int nk = (i1 - i0) + 2 * rad;
+        for (int t = tid; t < nk; t += SEL_THREADS) {
+            const int k = k0 + t;
+            raw[t] = (k >= 0 && k < n_sc) ? c0[k] + c1[k] : -__builtin_huge_valf();
+        }
+        __syncthreads();
+        for (int i = i0 + tid; i < i1; i += SEL_THREADS) {
+            const int t = i - i0 + rad;          // raw index of position L_sink + i
+            float mx = raw[t - rad];
+            for (int d = -rad + 1; d <= rad; ++d) mx = fmaxf(mx, raw[t + d]);
+            vals[i] = __float_as_uint(mx);
+        }
+    } else {
+        for (int i = i0 + tid; i < i1; i += SEL_THREADS) {
+            const int j = c.L_sink + i;
+            const int lo = max(0, j - rad), hi = min(n_sc - 1, j + rad);
+            float mx = c0[lo] + c1[lo];
+            for (int k = lo + 1; k <= hi; ++k) mx = fmaxf(mx, c0[k] + c1[k]);
+            vals[i] = __float_as_uint(mx);
+        }
     }
     if (tid == 0) {
         sh_prefix = 0u;
@@ -131,7 +183,7 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
         for (int base = i0; base < i1; base += SEL_THREADS) {
             const int i = base + tid;
             const bool in = i < i1;
-            const uint32_t v = in ? pool[i] : 0u;
+            const uint32_t v = in ? vals[i] : 0u;
             const bool match = in && (v & mask) == prefix;
             const unsigned active = __ballot_sync(0xffffffffu, match);
             if (match) {
@@ -142,27 +194,32 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
         }
         __syncthreads();
         int* hc = hist_cta[pass & 1];
-        for (int d = tid; d < 256; d += SEL_THREADS) {
+        if (tid < 256) {
             int t = 0;
-            for (int w = 0; w < SEL_WARPS; ++w) t += hist_w[w][d];
-            hc[d] = t;
+#pragma unroll 8
+            for (int w = 0; w < SEL_WARPS; ++w) t += hist_w[w][tid];
+            hc[tid] = t;
         }
         cluster.sync();                          // every CTA's histogram of this pass is ready
-        __shared__ int hist_all[256];
-        for (int d = tid; d < 256; d += SEL_THREADS) {
+        if (tid < 256) {
             int t = 0;
-            for (int r = 0; r < SEL_CLUSTER; ++r) t += cluster.map_shared_rank(hc, r)[d];
-            hist_all[d] = t;
+#pragma unroll
+            for (int r = 0; r < SEL_CLUSTER; ++r) t += cluster.map_shared_rank(hc, r)[tid];
+            hist_all[tid] = t;
         }
         __syncthreads();
-        if (tid == 0) {
-            int kk = sh_kk, cum = 0, d = 255;
-            for (; d > 0; --d) {
-                if (cum + hist_all[d] >= kk) break;
-                cum += hist_all[d];
+        if (warp == 0) {
+            int d = 0, kk = 0;
+            find_digit(hist_all, sh_kk, &d, &kk);
+            // exactly one lane found the digit; hand it to the block
+            const unsigned who = __ballot_sync(0xffffffffu, kk > 0);
+            const int src = who ? __ffs(who) - 1 : 0;
+            d = __shfl_sync(0xffffffffu, d, src);
+            kk = __shfl_sync(0xffffffffu, kk, src);
+            if (lane == 0) {
+                sh_kk = kk;
+                sh_prefix = prefix | ((uint32_t)d << shift);
             }
-            sh_kk = kk - cum;
-            sh_prefix = prefix | ((uint32_t)d << shift);
         }
         mask |= 255u << shift;
         __syncthreads();
@@ -175,7 +232,7 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
     const int r0 = min(i1, i0 + tid * run), r1 = min(i1, r0 + run);
     int gt = 0, eq = 0;
     for (int i = r0; i < r1; ++i) {
-        const uint32_t v = pool[i];
+        const uint32_t v = vals[i];
         gt += v > tau;
         eq += v == tau;
     }
@@ -202,7 +259,7 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
     int pos = taken_prev + gt_before + min(max(kk - eq_prev, 0), eq_before);
     int e_seen = eq_g;
     for (int i = r0; i < r1; ++i) {
-        const uint32_t v = pool[i];
+        const uint32_t v = vals[i];
         bool take = v > tau;
         if (v == tau) {
             take = e_seen < kk;
@@ -244,8 +301,17 @@ cudaError_t launch_lse_merge(const CompressArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_select(const CompressArgs& a, cudaStream_t st) {
+    // pooled values (and the raw column sums they come from) of one CTA's slice in
+    // shared memory when they fit next to the histograms, else in the workspace
+    constexpr int DYN_MAX = 150 * 1024;
+    static std::atomic<uint64_t> smem_set{0};
+    const int M = a.R0 - a.cfg.L_sink;
+    const int per = (M + SEL_CLUSTER - 1) / SEL_CLUSTER;
+    const long long bytes = 4ll * (2ll * per + 2 * (a.cfg.P / 2));
+    const int in_smem = bytes <= DYN_MAX;
+    if (cudaError_t e = opt_in_smem(select_kernel, DYN_MAX, smem_set); e != cudaSuccess) return e;
     dim3 grid(SEL_CLUSTER, a.cfg.Hkv);
-    select_kernel<<<grid, SEL_THREADS, 0, st>>>(a);
+    select_kernel<<<grid, SEL_THREADS, in_smem ? (size_t)bytes : 0, st>>>(a, in_smem);
     return cudaGetLastError();
 }
 
