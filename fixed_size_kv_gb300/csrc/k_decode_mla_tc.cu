@@ -59,14 +59,15 @@ constexpr int OFF_BAR = OFF_ML + 1536;
 constexpr int SMEM = OFF_BAR + 256 + 1024;                // barriers + alignment slack
 
 enum {
-    B_Q_FULL = 0,
+    B_Q_FULL = 0,                // q chunks 0..3 moved into TMEM (and 4..8 in place)
     B_KV_FULL = 1,               // + KST
     B_KV_EMPTY = 1 + KST,        // + KST
     B_S_FULL = 1 + 2 * KST,      // + NG: scores of the group's tile are in TMEM
     B_SP_EMPTY = 3 + 2 * KST,    // + NG: P V of the group's previous tile done (buffer free)
     B_P_FULL = 5 + 2 * KST,      // + NG: weights of the group's tile are in TMEM
     B_M_READY = 7 + 2 * KST,     // + 4 (one per lane quarter)
-    N_BARS = 11 + 2 * KST
+    B_Q_LOAD = 11 + 2 * KST,     // the TMA load of q (all nine chunks) has landed
+    N_BARS = 12 + 2 * KST
 };
 static_assert((N_BARS + 1) * 8 <= 256, "barrier area");
 static_assert(SMEM <= 232448, "shared memory");
@@ -80,8 +81,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV, DecodeArgs a) {
-    pdl_wait();                 // the append (or whatever produced q) has completed
+    mla_decode_tc_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ CUtensorMap tmQ,
+                         DecodeArgs a) {
     pdl_launch_dependents();    // the merge may launch once the last wave has started
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -99,10 +100,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     float* m_sh = reinterpret_cast<float*>(smem + OFF_ML);         // running max handed between groups
     float* l_sh = m_sh + HEADS;                                    // [NG][HEADS] group sums at the end
 
-    const int slot = a.slots[b];
-    const bool slot_ok = slot >= 0 && slot < c.max_batch;
-
     if (threadIdx.x == 0) {
+        mbar_init(bar(B_Q_LOAD), 1);
         mbar_init(bar(B_Q_FULL), NG * 4);      // the softmax warps, after storing q
         for (int i = 0; i < KST; ++i) {
             mbar_init(bar(B_KV_FULL + i), 1);
@@ -121,8 +120,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_alloc(smem_u32(tmem_holder), 512);
         tmem_relinquish();
     }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch(&tmKV);
+        tma_prefetch(&tmQ);
+    }
     __syncthreads();
     tc_fence_after();
+    // set-up above overlaps the previous kernel; from here on this kernel reads what
+    // earlier kernels wrote (the cache, its meta, q)
+    pdl_wait();
+    const int slot = a.slots[b];
+    const bool slot_ok = slot >= 0 && slot < c.max_batch;
     const uint32_t tmem = *tmem_holder;
     // TMEM: scores, then weights (one 64-column buffer per group), q chunks 0..3, O
     const uint32_t T_S = tmem, T_Q = tmem + 128, T_O = tmem + 256;
@@ -156,7 +164,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         m.T += 1;
         __syncthreads();            // every thread has read the meta; the row is written
-        if (threadIdx.x == 0) {
+        if (threadIdx.x == 33) {    // an idle lane of the MMA warp (not the TMA or MMA thread)
             __threadfence();
             if (atomicAdd(&a.meta_rw[slot].pad[0], 1) == (int)gridDim.x - 1) {   // 2 x splits CTAs
                 a.meta_rw[slot].T = m.T;
@@ -173,17 +181,28 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0 && t_begin < t_end) {
-            tma_prefetch(&tmKV);
+            // q, one TMA box per 64-column chunk: chunks 4..8 straight to their place, chunks
+            // 0..3 staged in the second KV stage until the softmax warps move them to TMEM
+            mbar_expect_tx(bar(B_Q_LOAD), NCH * QCH_B);
+            for (int j = 0; j < NCH; ++j) {
+                const uint32_t dst = j < QT_CH ? s_kv + NCH * CH_B + j * QCH_B : s_q + (j - QT_CH) * QCH_B;
+                tma_load_3d(dst, &tmQ, bar(B_Q_LOAD), 64 * j, 0, b);
+            }
             constexpr int AHEAD = 4;    // tiles on their way to L2 ahead of the loads
-            for (int t = t_begin; t < min(t_end, t_begin + AHEAD); ++t)
-                for (int j = 0; j < NCH; ++j) tma_prefetch_3d(&tmKV, 64 * j, t * TK, slot);
             int i = 0;
             for (int t = next_tile(t_begin); t < t_end; t = next_tile(t + 1), ++i) {
                 cur_tile = t;
-                if (t + AHEAD < t_end)
+                // the first stages' loads go out before any L2 prefetch; then the prefetch
+                // runs AHEAD tiles in front of the loads
+                if (i == KST)
+                    for (int u = t; u < min(t_end, t + AHEAD); ++u)
+                        for (int j = 0; j < NCH; ++j) tma_prefetch_3d(&tmKV, 64 * j, u * TK, slot);
+                if (i >= KST && t + AHEAD < t_end)
                     for (int j = 0; j < NCH; ++j) tma_prefetch_3d(&tmKV, 64 * j, (t + AHEAD) * TK, slot);
                 const int st = i % KST;
                 const uint32_t n = i / KST;
+                // the second stage holds q's staged chunks until they are in TMEM
+                if (i == 1 && !wait_bar(bar(B_Q_FULL), 0, abort_flag)) { fail(0); break; }
                 if (!wait_bar(bar(B_KV_EMPTY + st), (n & 1) ^ 1, abort_flag)) { fail(0); break; }
                 mbar_expect_tx(bar(B_KV_FULL + st), NCH * CH_B);
                 for (int j = 0; j < NCH; ++j)
@@ -211,22 +230,25 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int t = next_tile(t_begin); t < t_end; t = next_tile(t + 1)) ++n_t;
             int qk = 0, pv = 0;
             uint64_t t_idle = 0;
-            while (ok && pv < n_t) {
-                bool progressed = false;
-                if (pv < qk && mbar_test_wait(bar(B_P_FULL + (pv & 1)), (pv >> 1) & 1)) {
-                    tc_fence_after();
-                    const int stp = pv % KST;
-                    const uint32_t pa = T_S + (pv & 1) * TK;  // the weights, written over the scores
-                    const uint64_t vd = v_desc0 + (uint64_t)stp * ST16;
-                    tc_mma_ta(T_O, pa, vd, id_pv, pv > 0 ? 1u : 0u);
+            // P V of the oldest tile whose weights are ready, first (it frees a KV stage for
+            // the next load), else the scores of the next tile
+            auto try_pv = [&]() -> bool {
+                if (!(pv < qk && mbar_test_wait(bar(B_P_FULL + (pv & 1)), (pv >> 1) & 1))) return false;
+                tc_fence_after();
+                const int stp = pv % KST;
+                const uint32_t pa = T_S + (pv & 1) * TK;  // the weights, written over the scores
+                const uint64_t vd = v_desc0 + (uint64_t)stp * ST16;
+                tc_mma_ta(T_O, pa, vd, id_pv, pv > 0 ? 1u : 0u);
 #pragma unroll
-                    for (int k = 1; k < TK / 16; ++k)       // 16 keys (8 TMEM columns of P) per step
-                        tc_mma_ta(T_O, pa + k * 8, vd + (uint64_t)k * (2048 >> 4), id_pv, 1u);
-                    tc_commit(bar(B_SP_EMPTY + (pv & 1)));
-                    tc_commit(bar(B_KV_EMPTY + stp));
-                    ++pv;
-                    progressed = true;
-                }
+                for (int k = 1; k < TK / 16; ++k)       // 16 keys (8 TMEM columns of P) per step
+                    tc_mma_ta(T_O, pa + k * 8, vd + (uint64_t)k * (2048 >> 4), id_pv, 1u);
+                tc_commit(bar(B_SP_EMPTY + (pv & 1)));
+                tc_commit(bar(B_KV_EMPTY + stp));
+                ++pv;
+                return true;
+            };
+            while (ok && pv < n_t) {
+                bool progressed = try_pv();
                 if (!progressed && qk < n_t && mbar_test_wait(bar(B_SP_EMPTY + (qk & 1)), ((qk >> 1) & 1) ^ 1) &&
                     mbar_test_wait(bar(B_KV_FULL + qk % KST), (qk / KST) & 1)) {
                     tc_fence_after();
@@ -235,13 +257,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint64_t kd = kv_desc0 + (uint64_t)st * ST16;
                     tc_mma_ta(d, T_Q, kd, id_qk, 0u);
 #pragma unroll
-                    for (int i = 1; i < 4 * QT_CH; ++i)      // q chunks 0..3 from TMEM; 16 columns
+                    for (int i = 1; i < 4 * QT_CH; ++i) {    // q chunks 0..3 from TMEM; 16 columns
                         tc_mma_ta(d, T_Q + (i >> 2) * 32 + (i & 3) * 8,   // (8 TMEM columns of q) per step
                                   kd + (uint64_t)((i >> 2) * CH16 + (i & 3) * 2), id_qk, 1u);
+                    }
 #pragma unroll
-                    for (int i = 4 * QT_CH; i < 4 * NCH; ++i) // q chunks 4..8 from shared memory
+                    for (int i = 4 * QT_CH; i < 4 * NCH; ++i) { // q chunks 4..8 from shared memory
                         tc_mma(d, q_desc + (uint64_t)(((i >> 2) - QT_CH) * QCH16 + (i & 3) * 2),
                                kd + (uint64_t)((i >> 2) * CH16 + (i & 3) * 2), id_qk, 1u);
+                    }
                     tc_commit(bar(B_S_FULL + sb));
                     ++qk;
                     progressed = true;
@@ -250,7 +274,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     t_idle = 0;
                 } else if (t_idle == 0) {
                     t_idle = globaltimer_ns();
-                } else if (globaltimer_ns() - t_idle > WAIT_NS || *abort_flag) {
+                } else if (__nanosleep(20), globaltimer_ns() - t_idle > WAIT_NS || *abort_flag) {
                     cur_tile = pv;
                     fail(qk < n_t ? 11 : 13);
                     ok = false;
@@ -268,35 +292,35 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t m_ready = bar(B_M_READY + quarter);
         bool ok = true;
 
-        // q: chunks 0..3 into TMEM (one head per lane), chunks 4..8 into shared memory as
-        // 128-byte swizzled K-major tiles; the two groups take alternate chunks.
+        // q: the TMA load put chunks 4..8 in place (128-byte swizzled K-major tiles) and
+        // staged chunks 0..3 in the second KV stage; each lane moves its head's row of a
+        // staged chunk into TMEM (the two groups take alternate chunks)
         {
-            const bf16* qrow = a.q + ((size_t)b * c.Hq + row) * (size_t)c.dqk;
-            for (int j = g; j < NCH; j += NG) {
-                const uint4* src = reinterpret_cast<const uint4*>(qrow + 64 * j);
-                if (j < QT_CH) {
-                    float v[32];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const uint4 u = src[e];
-                        v[4 * e] = __uint_as_float(u.x);
-                        v[4 * e + 1] = __uint_as_float(u.y);
-                        v[4 * e + 2] = __uint_as_float(u.z);
-                        v[4 * e + 3] = __uint_as_float(u.w);
-                    }
-                    tmem_st32(T_Q + lane_off + 32 * j, v);
-                } else {
-                    const uint32_t dst = s_q + (j - QT_CH) * QCH_B + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const uint4 u = src[e];
-                        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(dst + ((e ^ (row & 7)) << 4)),
-                                     "r"(u.x), "r"(u.y), "r"(u.z), "r"(u.w)
-                                     : "memory");
-                    }
-                }
+            bool qok = true;
+            if (t_begin < t_end)
+                qok = __all_sync(0xffffffffu, wait_bar(bar(B_Q_LOAD), 0, abort_flag));
+            if (!qok) {
+                fail(2);
+                ok = false;
             }
-            fence_proxy_async();
+            for (int j = g; qok && t_begin < t_end && j < QT_CH; j += NG) {
+                const uint32_t src = s_kv + NCH * CH_B + j * QCH_B + (row >> 3) * 1024 + (row & 7) * 128;
+                float v[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    uint32_t x, y, z, w;
+                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
+                                 : "=r"(x), "=r"(y), "=r"(z), "=r"(w)
+                                 : "r"(src + ((e ^ (row & 7)) << 4))
+                                 : "memory");
+                    v[4 * e] = __uint_as_float(x);
+                    v[4 * e + 1] = __uint_as_float(y);
+                    v[4 * e + 2] = __uint_as_float(z);
+                    v[4 * e + 3] = __uint_as_float(w);
+                }
+                tmem_st32(T_Q + lane_off + 32 * j, v);
+            }
+            fence_proxy_async();    // the staged chunks were read before the stage is reloaded
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -310,6 +334,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             if ((i & 1) != g || !ok) continue;
             cur_tile = t;
             const int k_g = i >> 1;             // this group's k-th tile: barrier phase parity k_g & 1
+            // 0. which of the tile's 64 slots are valid (two ballots), before its scores exist
+            const uint32_t v0 = __ballot_sync(0xffffffffu, t * TK + lane < c.C && sv.valid(t * TK + lane));
+            const uint32_t v1 =
+                __ballot_sync(0xffffffffu, t * TK + 32 + lane < c.C && sv.valid(t * TK + 32 + lane));
             // 1. the scores of tile i, out of TMEM
             float s[TK];
             if (!__all_sync(0xffffffffu, wait_bar(bar(B_S_FULL + g), k_g & 1, abort_flag))) {
@@ -330,10 +358,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     s[32 + k] = hi[k];
                 }
             }
-            // 2. mask (two ballots for the tile's 64 slots), scale, tile max
-            const uint32_t v0 = __ballot_sync(0xffffffffu, t * TK + lane < c.C && sv.valid(t * TK + lane));
-            const uint32_t v1 =
-                __ballot_sync(0xffffffffu, t * TK + 32 + lane < c.C && sv.valid(t * TK + 32 + lane));
+            // 2. mask, scale, tile max
             float mt = NEG_INF;
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
@@ -393,18 +418,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             // 5. weights (bf16, two keys per TMEM column) over this group's scores (read
             //    above, so the buffer is free until P V of this tile releases it)
             float w[32];
-            float psum = 0.f;
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};     // independent partial sums
+            const float m_sub = m_new == NEG_INF ? 0.f : m_new;   // all scores -inf then: weights 0
 #pragma unroll
             for (int e = 0; e < TK / 2; ++e) {
-                const float p0 = m_new == NEG_INF ? 0.f : bf16_round(ex2(s[2 * e] - m_new));
-                const float p1 = m_new == NEG_INF ? 0.f : bf16_round(ex2(s[2 * e + 1] - m_new));
-                psum += p0 + p1;
-                w[e] = __uint_as_float(pack_bf16(p0, p1));
+                // one conversion per pair; the sum takes the rounded weights back out of
+                // the packed word with integer ops
+                const uint32_t pk = pack_bf16(ex2(s[2 * e] - m_sub), ex2(s[2 * e + 1] - m_sub));
+                ps[e & 3] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xffff0000u);
+                w[e] = __uint_as_float(pk);
             }
             tmem_st32(t_buf, w);
             tmem_st_wait();
             tc_fence_before();
-            l_g += psum;
+            l_g += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_P_FULL + g));
         }
@@ -496,10 +523,11 @@ int mla_decode_wave_ctas() {
     return per_sm * sms;
 }
 
-cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cudaStream_t st) {
+cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, const CUtensorMap& tq,
+                                 cudaStream_t st) {
     if (cudaError_t e = opt_in_smem(mla_decode_tc_kernel, SMEM, mla_smem_set); e != cudaSuccess) return e;
     dim3 grid(2 * a.splits, a.n);
-    return launch_dependent(mla_decode_tc_kernel, grid, dim3(THREADS), SMEM, st, tkv, a);
+    return launch_dependent(mla_decode_tc_kernel, grid, dim3(THREADS), SMEM, st, tkv, tq, a);
 }
 
 }  // namespace snap

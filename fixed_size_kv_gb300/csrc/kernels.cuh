@@ -75,8 +75,9 @@ cudaError_t opt_in_smem(void (*kernel)(Exp...), int bytes, std::atomic<uint64_t>
 }
 
 cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st);
-// tkv: cache [max_batch][C][576], box {64, 64, 1} (queries are read from a.q directly)
-cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, cudaStream_t st);
+// tkv: cache [max_batch][C][576], box {64, 64, 1}; tq: queries [n][128][576], box {64, 128, 1}
+cudaError_t launch_decode_mla_tc(const DecodeArgs& a, const CUtensorMap& tkv, const CUtensorMap& tq,
+                                 cudaStream_t st);
 // CTAs of the MLA decode kernel that can be resident at once on the current device
 // (one per SM at its shared-memory size; 0 if the occupancy query fails).
 int mla_decode_wave_ctas();

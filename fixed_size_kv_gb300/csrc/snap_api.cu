@@ -355,9 +355,14 @@ cudaError_t run_decode(snap_cache* cache, DecodeArgs& a, cudaStream_t st) {
     a.meta_rw = cache->meta;
     a.merge_cnt = cache->merge_cnt;
     if (cache->cfg.layout == SNAP_LAYOUT_GQA) return launch_decode_gqa(a, st);
-    CUtensorMap tkv;
+    CUtensorMap tkv, tq;
     if (!mla_cache_map(&tkv, cache)) return cudaErrorInvalidValue;
-    cudaError_t e = launch_decode_mla_tc(a, tkv, st);
+    const snap_config& c = cache->cfg;
+    const cuuint64_t qd[3] = {(cuuint64_t)c.d_qk, (cuuint64_t)c.n_q_heads, (cuuint64_t)a.n};
+    const cuuint64_t qs[2] = {(cuuint64_t)c.d_qk * 2, (cuuint64_t)c.n_q_heads * c.d_qk * 2};
+    const cuuint32_t qb[3] = {64, (cuuint32_t)c.n_q_heads, 1};
+    if (!encode(&tq, a.q, 3, qd, qs, qb)) return cudaErrorInvalidValue;
+    cudaError_t e = launch_decode_mla_tc(a, tkv, tq, st);
     if (e == cudaSuccess && a.splits > 1) e = launch_decode_merge(a, st);
     return e;
 }
