@@ -299,7 +299,8 @@ def test_gqa_decode_step_is_one_launch(C_parts, lengths):
     tok = inputs.gen_decode(wl, len(lengths), step=0, seed=19)
     q, k, v = tok.q.cuda(), tok.k.cuda(), tok.v.cuda()
     b.cache.decode_step(b.dslots, q, k, v)         # first call: one-time set-up outside the profile
-    names = _kernels_of(lambda: b.cache.decode_step(b.dslots, q, k, v))
+    _kernels_of(lambda: torch.zeros(1, device="cuda").add_(1))   # the profiler's own first-use set-up
+    names = _kernels_of(lambda: [b.cache.decode_step(b.dslots, q, k, v) for _ in range(3)])
     if not names:
         pytest.skip("the profiler reported no kernels on this box")
-    assert names == ["gqa_decode_kernel"] or (len(names) == 1 and "gqa_decode_kernel" in names[0]), (splits, names)
+    assert len(names) == 3 and all("gqa_decode_kernel" in n for n in names), (splits, names)
