@@ -145,8 +145,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (!waitb(bar(B_KV_FULL + st), (j >> 1) & 1, abort_flag)) { fail(11); break; }
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j > qt0 + t || (t == 1 && !valid1)) continue;
-                    // the S buffer holds P of the previous key tile until its P V is done
-                    if (j > 0 && !waitb(bar(B_PV_DONE + t), (j - 1) & 1, abort_flag)) { fail(12); ok = false; break; }
+                    // The S buffer holds P of the previous key tile, read by that tile's P V;
+                    // this S is issued after that P V on the same thread, and tcgen05.mma
+                    // operations of one thread execute in issue order, so it writes the
+                    // buffer only after the P V has read it.  (The softmax had finished
+                    // reading the previous scores before it signalled their weights.)
                     tc_fence_after();
                     const uint32_t d = tmem + t * 128;
                     const uint64_t qa = q_desc + (uint64_t)(t * 2) * CH16;
@@ -185,6 +188,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t tO = tmem + 256 + t * 128 + lane_off;
         const float sl2 = a.sl2;
         const bool active = t == 0 || valid1;
+        // the unrounded sum feeds only the log-sum-exp of the last W rows
+        const bool need_lse = a.lse_obs != nullptr && __any_sync(0xffffffffu, row >= a.S - a.W && row < a.S);
         float m_used = NEG_INF, l_bf = 0.f, l_ex = 0.f;
         bool ok = true;
         for (int j = 0; active && ok && j <= qt; ++j) {
@@ -205,11 +210,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld32(tS + c * 32, v);
                 tmem_ld_wait(v);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float s = (diag && key0 + c * 32 + e > row) ? NEG_INF : v[e] * sl2;
-                    mx = fmaxf(mx, s);
-                }
+                for (int e = 0; e < 32; ++e)
+                    mx = fmaxf(mx, (diag && key0 + c * 32 + e > row) ? NEG_INF : v[e]);
             }
+            mx *= sl2;                                   // sl2 > 0: the max of the scaled scores
             // lazy running max; O is rescaled (warp-wide, tcgen05 is warp-collective) when
             // a lane's max moves and its old max was finite, after P V of the last tile
             const bool move = mx > m_used + RESCALE_GAP || (m_used == NEG_INF && mx != NEG_INF);
@@ -249,28 +253,33 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld_wait(lo);
                 tmem_ld_wait(hi);
                 float w[32];
+                if (diag) {                      // the tile that crosses the causal limit
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        if (key0 + c2 * 64 + e > row) lo[e] = NEG_INF;
+                        if (key0 + c2 * 64 + 32 + e > row) hi[e] = NEG_INF;
+                    }
+                }
+                const float nm = -m_used;
+                float sb[4] = {0.f, 0.f, 0.f, 0.f}, se[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int k0 = key0 + c2 * 64 + 2 * e;
-                    const float s0 = (diag && k0 > row) ? NEG_INF : lo[2 * e] * sl2;
-                    const float s1 = (diag && k0 + 1 > row) ? NEG_INF : lo[2 * e + 1] * sl2;
-                    const float p0 = ex2(s0 - m_used), p1 = ex2(s1 - m_used);
-                    const float b0 = bf16_round(p0), b1 = bf16_round(p1);
-                    l_ex += p0 + p1;
-                    l_bf += b0 + b1;
-                    w[e] = __uint_as_float(pack_bf16(p0, p1));
+                    const float p0 = ex2(fmaf(lo[2 * e], sl2, nm)), p1 = ex2(fmaf(lo[2 * e + 1], sl2, nm));
+                    const uint32_t pk = pack_bf16(p0, p1);   // the weights P V uses
+                    sb[e & 3] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xffff0000u);
+                    if (need_lse) se[e & 3] += p0 + p1;
+                    w[e] = __uint_as_float(pk);
                 }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int k0 = key0 + c2 * 64 + 32 + 2 * e;
-                    const float s0 = (diag && k0 > row) ? NEG_INF : hi[2 * e] * sl2;
-                    const float s1 = (diag && k0 + 1 > row) ? NEG_INF : hi[2 * e + 1] * sl2;
-                    const float p0 = ex2(s0 - m_used), p1 = ex2(s1 - m_used);
-                    const float b0 = bf16_round(p0), b1 = bf16_round(p1);
-                    l_ex += p0 + p1;
-                    l_bf += b0 + b1;
-                    w[16 + e] = __uint_as_float(pack_bf16(p0, p1));
+                    const float p0 = ex2(fmaf(hi[2 * e], sl2, nm)), p1 = ex2(fmaf(hi[2 * e + 1], sl2, nm));
+                    const uint32_t pk = pack_bf16(p0, p1);
+                    sb[e & 3] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xffff0000u);
+                    if (need_lse) se[e & 3] += p0 + p1;
+                    w[16 + e] = __uint_as_float(pk);
                 }
+                l_bf += (sb[0] + sb[1]) + (sb[2] + sb[3]);
+                l_ex += (se[0] + se[1]) + (se[2] + se[3]);
                 tmem_st32(tS + c2 * 32, w);
             }
             tmem_st_wait();
