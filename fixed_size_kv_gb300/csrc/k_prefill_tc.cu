@@ -139,41 +139,73 @@ __global__ void __launch_bounds__(THREADS, 1)
             constexpr uint64_t CH16 = CHB >> 4, ST16 = STAGE_B >> 4;
             bool ok = waitb(bar(B_Q_FULL), 0, abort_flag);
             if (!ok) fail(10);
+            // Issue order (ping-pong of the two query tiles): S_0(0) S_1(0), then per key
+            // tile j: P V_0(j), S_0(j+1), P V_1(j), S_1(j+1).  Each score MMA group goes in
+            // as soon as its tile's previous weights are consumed, so one group's softmax
+            // overlaps the other group's MMAs.
+            // The S buffer holds P of the previous key tile, read by that tile's P V; the
+            // next S is issued after that P V on the same thread, and tcgen05.mma operations
+            // of one thread execute in issue order, so it writes the buffer only after the
+            // P V has read it.  (The softmax had finished reading the previous scores before
+            // it signalled their weights.)
+            auto active_at = [&](int t, int j) { return j <= qt0 + t && (t == 0 || valid1) && j <= J; };
+            auto issue_s = [&](int t, int j) {
+                const int st = j & 1;
+                const uint32_t d = tmem + t * 128;
+                const uint64_t qa = q_desc + (uint64_t)(t * 2) * CH16;
+                const uint64_t kb = k_desc + (uint64_t)st * ST16;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma(d, qa + (uint64_t)((kk >> 2) * CH16 + (kk & 3) * 2),
+                           kb + (uint64_t)((kk >> 2) * CH16 + (kk & 3) * 2), id_s, kk > 0 ? 1u : 0u);
+                tc_commit(bar(B_S_FULL + t));
+            };
+            auto issue_pv = [&](int t, int j) {
+                const int st = j & 1;
+                const uint32_t pa = tmem + t * 128;
+                const uint32_t o = tmem + 256 + t * 128;
+                const uint64_t vb = v_desc + (uint64_t)st * ST16;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)      // 16 keys (8 TMEM columns of P) per MMA
+                    tc_mma_ta(o, pa + kk * 8, vb + (uint64_t)kk * (2048 >> 4), id_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar(B_PV_DONE + t));
+            };
+            if (ok) {
+                if (!waitb(bar(B_KV_FULL + 0), 0, abort_flag)) {
+                    fail(11);
+                    ok = false;
+                } else {
+                    tc_fence_after();
+                    issue_s(0, 0);
+                    if (active_at(1, 0)) issue_s(1, 0);
+                }
+            }
             for (int j = 0; ok && j <= J; ++j) {
                 cur = j;
                 const int st = j & 1;
-                if (!waitb(bar(B_KV_FULL + st), (j >> 1) & 1, abort_flag)) { fail(11); break; }
+                // the next key tile (its scores follow each P V below)
+                const bool next = j + 1 <= J;
+                bool next_ready = false;
                 for (int t = 0; t < 2 && ok; ++t) {
-                    if (j > qt0 + t || (t == 1 && !valid1)) continue;
-                    // The S buffer holds P of the previous key tile, read by that tile's P V;
-                    // this S is issued after that P V on the same thread, and tcgen05.mma
-                    // operations of one thread execute in issue order, so it writes the
-                    // buffer only after the P V has read it.  (The softmax had finished
-                    // reading the previous scores before it signalled their weights.)
-                    tc_fence_after();
-                    const uint32_t d = tmem + t * 128;
-                    const uint64_t qa = q_desc + (uint64_t)(t * 2) * CH16;
-                    const uint64_t kb = k_desc + (uint64_t)st * ST16;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        tc_mma(d, qa + (uint64_t)((kk >> 2) * CH16 + (kk & 3) * 2),
-                               kb + (uint64_t)((kk >> 2) * CH16 + (kk & 3) * 2), id_s, kk > 0 ? 1u : 0u);
-                    tc_commit(bar(B_S_FULL + t));
+                    if (active_at(t, j)) {
+                        if (!waitb(bar(B_P_FULL + t), j & 1, abort_flag)) { fail(13); ok = false; break; }
+                        tc_fence_after();
+                        issue_pv(t, j);
+                    }
+                    if (next && active_at(t, j + 1)) {
+                        if (!next_ready) {
+                            if (!waitb(bar(B_KV_FULL + ((j + 1) & 1)), ((j + 1) >> 1) & 1, abort_flag)) {
+                                fail(11);
+                                ok = false;
+                                break;
+                            }
+                            next_ready = true;
+                            tc_fence_after();
+                        }
+                        issue_s(t, j + 1);
+                    }
                 }
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j > qt0 + t || (t == 1 && !valid1)) continue;
-                    if (!waitb(bar(B_P_FULL + t), j & 1, abort_flag)) { fail(13); ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t pa = tmem + t * 128;
-                    const uint32_t o = tmem + 256 + t * 128;
-                    const uint64_t vb = v_desc + (uint64_t)st * ST16;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)      // 16 keys (8 TMEM columns of P) per MMA
-                        tc_mma_ta(o, pa + kk * 8, vb + (uint64_t)kk * (2048 >> 4), id_pv,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar(B_PV_DONE + t));
-                }
-                tc_commit(bar(B_KV_EMPTY + st));
+                tc_commit(bar(B_KV_EMPTY + st));    // after both P V of key tile j
             }
         }
     } else {
