@@ -234,17 +234,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const bool diag = j == qt;                   // keys j*BN .. may pass the row
             const int key0 = j * BN;
-            // pass 1: the tile's row max
-            float mx = NEG_INF;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tmem_ld32(tS + c * 32, v);
-                tmem_ld_wait(v);
+            // the tile's 128 scores of this row, all in registers (one TMEM round trip)
+            float v[4][32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    mx = fmaxf(mx, (diag && key0 + c * 32 + e > row) ? NEG_INF : v[e]);
+            for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, v[c]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld_wait(v[c]);
+            if (diag) {                                  // the tile that crosses the causal limit
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (key0 + c * 32 + e > row) v[c][e] = NEG_INF;
             }
+            float mx = NEG_INF;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, v[c][e]);
             mx *= sl2;                                   // sl2 > 0: the max of the scaled scores
             // lazy running max; O is rescaled (warp-wide, tcgen05 is warp-collective) when
             // a lane's max moves and its old max was finite, after P V of the last tile
@@ -276,22 +283,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 l_ex *= alpha;
                 m_used = m_new;
             }
-            // pass 2: weights, bf16 pairs written over the scores (64 columns)
-#pragma unroll 1
-            for (int c2 = 0; c2 < 2; ++c2) {
-                float lo[32], hi[32];
-                tmem_ld32(tS + c2 * 64, lo);
-                tmem_ld32(tS + c2 * 64 + 32, hi);
-                tmem_ld_wait(lo);
-                tmem_ld_wait(hi);
-                float w[32];
-                if (diag) {                      // the tile that crosses the causal limit
+            // weights, bf16 pairs written over the scores (64 columns)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        if (key0 + c2 * 64 + e > row) lo[e] = NEG_INF;
-                        if (key0 + c2 * 64 + 32 + e > row) hi[e] = NEG_INF;
-                    }
-                }
+            for (int c2 = 0; c2 < 2; ++c2) {
+                float (&lo)[32] = v[2 * c2];
+                float (&hi)[32] = v[2 * c2 + 1];
+                float w[32];
                 const float nm = -m_used;
                 float sb[4] = {0.f, 0.f, 0.f, 0.f}, se[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
