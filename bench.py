@@ -54,6 +54,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-full-kv", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--prefill-only", type=int, default=0, metavar="S",
+                   help="extra mode: only the prefill attention of one S-token prompt (profiling)")
     p.add_argument("--no-prefill", action="store_true",
                    help="skip the prefill-attention timing (compression as prefill overhead)")
     p.add_argument("--no-workloads", action="store_true",
@@ -357,6 +359,7 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
         stream.synchronize()
         evs = [ev]
     attn_ms = [sum(e["a0"][t].elapsed_time(e["a1"][t]) for t in range(D)) / D for e in evs]
+    eager_launch_ms = statistics.mean(attn_ms)
     st = cache.check_device(stream)
     if st != snap.SNAP_OK:
         raise RuntimeError(f"{wl.name}: device status after timed steps: {snap.status_string(st)}")
@@ -367,7 +370,10 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
     total_ms = reduce_max(sum(step_ms))
     dec_ms = reduce_max(sum(decode_ms)) / steps
     cmp_ms = reduce_max(sum(compress_ms)) / steps
-    attn_avg_ms = statistics.mean(attn_ms)
+    # the decode step's device time: from the graph-replayed loop (back-to-back launches, as
+    # the timed region runs them) when the loop is a graph, else per eager launch; a GQA step
+    # is one kernel, an MLA step the attention kernel plus its merge
+    attn_avg_ms = dec_ms / D if graph is not None else eager_launch_ms
     attn_gbs = attn_bytes / (attn_avg_ms / 1e3) / 1e9
 
     # ---------------------------------------------------------------- full-KV baseline
@@ -529,7 +535,9 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
             "compress_with_prefill_lse_ms_per_seq": cmp_lse_ms,
             "compress_stage_ms_per_seq": stage_ms,
             "attn": {"ms": attn_avg_ms, "hbm_gbs": attn_gbs, "bytes_per_launch": attn_bytes,
-                     "frac": attn_gbs / hbm_peak},
+                     "frac": attn_gbs / hbm_peak, "eager_launch_ms": eager_launch_ms,
+                     "timing": ("graph-replayed decode loop / steps" if graph is not None
+                                else "CUDA events around each eager launch")},
             "full_kv": full,
             "speedup_vs_full_kv": (B * D * world / (dec_ms / 1e3)) / full["decode_tok_s"] if full else None,
             "cache_bytes": snap.cache_bytes(cfg, B),
@@ -1151,10 +1159,43 @@ def run_sweep(args):
                           "note": "StreamingLLM only" if k == 0 else ""}), flush=True)
 
 
+def run_prefill_only(args):
+    """The prefill attention alone (profiling): snap_prefill_attn of one prompt of
+    --prefill-only tokens of the workload (GQA), with the window rows' LSE, run three
+    times; prints the CUDA-event time of the last two."""
+    import torch
+    from fixed_size_kv_gb300 import inputs, snap
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    snap.load(build_if_missing=True)
+    wl = inputs.WORKLOADS[args.workload]
+    S = args.prefill_only
+    pre = inputs.gen_prefill(wl, S, seed=args.seed, device=dev)
+    Q = inputs.gen_prompt_queries(wl, pre, seed=args.seed, device=dev)
+    cache = snap.SnapCache(snap.make_config(**wl.config_kwargs()), max_batch=1, max_prompt=1, device=dev)
+    lse = torch.empty((wl.W, wl.n_q_heads), dtype=torch.float32, device=dev)
+    O = torch.empty_like(Q)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(3)]
+    for a, b in ev:
+        a.record()
+        cache.prefill_attn(Q, pre.K, pre.V, O=O, lse_obs=lse)
+        b.record()
+    torch.cuda.synchronize()
+    if cache.check_device() != snap.SNAP_OK:
+        raise RuntimeError("device status after the prefill")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev[1:])
+    flop = 2.0 * wl.n_q_heads * wl.d_qk * S * (S + 1)
+    print(json.dumps({"mode": "prefill", "workload": wl.name, "prompt_len": S, "ms": ms,
+                      "tflops": flop / (ms / 1e3) / 1e12}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.prefill_only:
+        run_prefill_only(args)
         return
     if args.capacity > 0:
         run_capacity(args)
