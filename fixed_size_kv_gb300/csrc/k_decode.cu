@@ -34,56 +34,13 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
     pdl_wait();                 // the previous kernel on the stream has completed
     pdl_launch_dependents();    // the next step's kernel may set up (it waits for this grid)
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ snap_seq_meta m_sh;
     __shared__ int last_sh;
     const DevConfig& c = a.cfg;
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int slot = a.slots[b];
-    if (slot < 0 || slot >= c.max_batch) {
-        if (threadIdx.x == 0 && split == 0 && h == 0)
-            report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
-        if (split == 0)  // no CTA of this sequence goes on: split 0 writes the zero output
-            for (int i = threadIdx.x; i < c.G * GD; i += blockDim.x)
-                a.out[((size_t)b * c.Hq + (size_t)h * c.G) * GD + i] = 0.f;
-        return;
-    }
-    if (threadIdx.x == 0) m_sh = a.meta[slot];
-    __syncthreads();
-    snap_seq_meta m = m_sh;
-    const size_t row0 = ((size_t)slot * c.Hkv + h) * (size_t)c.C;
-    const bf16* kbase = a.kc + row0 * GD;
-    const bf16* vbase = a.vc + row0 * GD;
-    const int ntiles = (c.C + GQA_KEYS - 1) / GQA_KEYS;
-    const int t_begin = split * a.tiles_per_split;
-    const int t_end = min(ntiles, t_begin + a.tiles_per_split);
-    if (a.k_new) {
-        // fused ring append: the CTA whose key range holds the new token's ring slot
-        // writes its K/V row before reading any tile; the attention then sees T + 1
-        const int s_app = c.L_sink + c.K + m.T % c.L_recent;
-        if (s_app >= t_begin * GQA_KEYS && s_app < t_end * GQA_KEYS && threadIdx.x < 32) {
-            const bool isv = threadIdx.x >= 16;
-            const int ch = threadIdx.x & 15;
-            const uint4* src = reinterpret_cast<const uint4*>((isv ? a.v_new : a.k_new) + ((size_t)b * c.Hkv + h) * GD);
-            bf16* dst = const_cast<bf16*>(isv ? vbase : kbase) + (size_t)s_app * GD;
-            reinterpret_cast<uint4*>(dst)[ch] = src[ch];
-            __threadfence();
-        }
-        m.T += 1;
-        __syncthreads();
-        // the last CTA of the sequence to get here (every CTA has read the meta) advances T
-        if (threadIdx.x == 0) {
-            __threadfence();
-            const int total = gridDim.x * gridDim.y;   // splits x KV heads
-            if (atomicAdd(&a.meta_rw[slot].pad[0], 1) == total - 1) {
-                a.meta_rw[slot].T = m.T;
-                a.meta_rw[slot].pad[0] = 0;
-            }
-        }
-    }
-    SlotValidity sv;
-    sv.init(m, c);
 
+    // Loads that need neither the slot nor its meta go out first.
     // Q^T as B fragments: n = head (lane/4), k = d.
     uint32_t qf[8][2];
     {
@@ -99,13 +56,32 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
             }
         }
     }
+    // this lane's 16 bytes of the appended token: K row (lanes 0-15) or V row (16-31)
+    uint4 new_row = make_uint4(0u, 0u, 0u, 0u);
+    if (a.k_new)
+        new_row = reinterpret_cast<const uint4*>((lane < 16 ? a.k_new : a.v_new) +
+                                                 ((size_t)b * c.Hkv + h) * GD)[lane & 15];
 
+    if (slot < 0 || slot >= c.max_batch) {
+        if (threadIdx.x == 0 && split == 0 && h == 0)
+            report_error(a.status, SNAP_ERR_DEVICE_CHECK, 1, b, slot);
+        if (split == 0)  // no CTA of this sequence goes on: split 0 writes the zero output
+            for (int i = threadIdx.x; i < c.G * GD; i += blockDim.x)
+                a.out[((size_t)b * c.Hq + (size_t)h * c.G) * GD + i] = 0.f;
+        return;
+    }
+    // the sequence's meta (S, T, R0, n_sink, n_mid, pad): two 16-byte loads, used below
+    const int4* mp = reinterpret_cast<const int4*>(a.meta + slot);
+    const int4 m0 = mp[0], m1 = mp[1];
+
+    const size_t row0 = ((size_t)slot * c.Hkv + h) * (size_t)c.C;
+    const bf16* kbase = a.kc + row0 * GD;
+    const bf16* vbase = a.vc + row0 * GD;
+    const int ntiles = (c.C + GQA_KEYS - 1) / GQA_KEYS;
+    const int t_begin = split * a.tiles_per_split;
+    const int t_end = min(ntiles, t_begin + a.tiles_per_split);
     const uint32_t wsm = smem_u32(smem) + warp * G_STAGES * G_STAGE_BYTES;
 
-    auto next_tile = [&](int t) {
-        while (t < t_end && !sv.any_valid(t * GQA_KEYS, min(c.C, (t + 1) * GQA_KEYS))) t += G_WARPS;
-        return t;
-    };
     auto load_tile = [&](int t, int st) {
         const uint32_t sk = wsm + st * G_STAGE_BYTES;
         const uint32_t svv = sk + GQA_KEYS * G_ROWB;
@@ -119,6 +95,65 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
             cp_async16(svv + swz(r, ch, G_ROWB), vbase + off, ok ? 16 : 0);
         }
     };
+    // Speculative prologue: the warp's first G_STAGES - 1 tiles (every G_WARPS-th tile
+    // of the range) are requested while the meta is in flight; the validity walk below
+    // confirms them or reloads.
+#pragma unroll
+    for (int st = 0; st < G_STAGES - 1; ++st) {
+        const int t = t_begin + warp + st * G_WARPS;
+        if (t < t_end) load_tile(t, st);
+        cp_async_commit();
+    }
+
+    snap_seq_meta m;
+    m.S = m0.x;
+    m.T = m0.y;
+    m.R0 = m0.z;
+    m.n_sink = m0.w;
+    m.n_mid = m1.x;
+    // Fused ring append: the new token's ring slot s_app.  The warp that computes the
+    // tile holding it writes the row to the cache and patches it into its stage (its
+    // load may have read the old row); the attention sees T + 1 tokens.
+    int t_app = -1, s_app = 0;
+    if (a.k_new) {
+        s_app = c.L_sink + c.K + m.T % c.L_recent;
+        m.T += 1;
+        const int t = s_app / GQA_KEYS;
+        if (t >= t_begin && t < t_end && (t - t_begin) % G_WARPS == warp) {
+            t_app = t;
+            bf16* dst = const_cast<bf16*>(lane < 16 ? kbase : vbase) + (size_t)s_app * GD;
+            reinterpret_cast<uint4*>(dst)[lane & 15] = new_row;
+        }
+    }
+    SlotValidity sv;
+    sv.init(m, c);
+
+    auto next_tile = [&](int t) {
+        while (t < t_end && !sv.any_valid(t * GQA_KEYS, min(c.C, (t + 1) * GQA_KEYS))) t += G_WARPS;
+        return t;
+    };
+    // the tiles the warp computes: every G_WARPS-th tile with a valid slot
+    const int t_first = next_tile(t_begin + warp);
+    int t_load = t_first;
+    bool spec_ok = true;
+    int chain[G_STAGES - 1];
+#pragma unroll
+    for (int st = 0; st < G_STAGES - 1; ++st) {
+        chain[st] = t_load;
+        if (t_load < t_end) {
+            if (t_load != t_begin + warp + st * G_WARPS) spec_ok = false;
+            t_load = next_tile(t_load + G_WARPS);
+        }
+    }
+    if (!spec_ok) {             // a skipped tile: drop the speculative stages, load the walk's
+        cp_async_wait<0>();
+        __syncwarp();
+#pragma unroll
+        for (int st = 0; st < G_STAGES - 1; ++st) {
+            if (chain[st] < t_end) load_tile(chain[st], st);
+            cp_async_commit();
+        }
+    }
 
     float m_run[2] = {NEG_INF, NEG_INF};
     float l_run[2] = {0.f, 0.f};
@@ -126,16 +161,7 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
 #pragma unroll
     for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-    int t_load = next_tile(t_begin + warp);
-    int t_comp = t_load;
-#pragma unroll
-    for (int st = 0; st < G_STAGES - 1; ++st) {
-        if (t_load < t_end) {
-            load_tile(t_load, st);
-            t_load = next_tile(t_load + G_WARPS);
-        }
-        cp_async_commit();
-    }
+    int t_comp = t_first;
     int st_comp = 0, st_load = G_STAGES - 1;
     const float sl2 = c.scale_log2;
     while (t_comp < t_end) {
@@ -149,6 +175,13 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
 
         const uint32_t sk = wsm + st_comp * G_STAGE_BYTES;
         const uint32_t svv = sk + GQA_KEYS * G_ROWB;
+        if (t_comp == t_app) {  // the appended row replaces whatever the load read there
+            const uint32_t dst = (lane < 16 ? sk : svv) + swz(s_app - t_comp * GQA_KEYS, lane & 15, G_ROWB);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(new_row.x),
+                         "r"(new_row.y), "r"(new_row.z), "r"(new_row.w)
+                         : "memory");
+            __syncwarp();
+        }
         float s[2][4];
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
@@ -258,61 +291,97 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
     }
     __syncthreads();
     const int d = threadIdx.x;  // 128 threads == 128 dims
-    for (int hh = 0; hh < c.G; ++hh) {
-        float M = NEG_INF;
+    // this CTA's (max, sum, O[d]) per query head, kept for the split merge
+    float Mh[8], Lh[8], Oh[8];
 #pragma unroll
-        for (int w = 0; w < G_WARPS; ++w) M = fmaxf(M, mlb[(w * 8 + hh) * 2]);
-        float L = 0.f, O = 0.f;
-        if (M != NEG_INF) {
+    for (int hh = 0; hh < 8; ++hh) {
+        Mh[hh] = NEG_INF;
+        Lh[hh] = Oh[hh] = 0.f;
+        if (hh >= c.G) continue;
+#pragma unroll
+        for (int w = 0; w < G_WARPS; ++w) Mh[hh] = fmaxf(Mh[hh], mlb[(w * 8 + hh) * 2]);
+        if (Mh[hh] != NEG_INF) {
 #pragma unroll
             for (int w = 0; w < G_WARPS; ++w) {
-                const float f = ex2(mlb[(w * 8 + hh) * 2] - M);
-                L += f * mlb[(w * 8 + hh) * 2 + 1];
-                O += f * ob[(w * 8 + hh) * GD + d];
+                const float f = ex2(mlb[(w * 8 + hh) * 2] - Mh[hh]);
+                Lh[hh] += f * mlb[(w * 8 + hh) * 2 + 1];
+                Oh[hh] += f * ob[(w * 8 + hh) * GD + d];
             }
         }
-        if (a.splits == 1) {
-            const float r = L > 0.f ? O / L : 0.f;
-            a.out[((size_t)b * c.Hq + (size_t)h * c.G + hh) * GD + d] = r;
-        } else {
+        if (a.splits > 1) {
             const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + split) * c.G + hh;
-            a.part_o[pi * GD + d] = O;
+            a.part_o[pi * GD + d] = Oh[hh];
             if (d == 0) {
-                a.part_ml[pi * 2 + 0] = M;
-                a.part_ml[pi * 2 + 1] = L;
+                a.part_ml[pi * 2 + 0] = Mh[hh];
+                a.part_ml[pi * 2 + 1] = Lh[hh];
             }
         }
     }
-    if (a.splits == 1) return;
-    // split merge in the last CTA of (sequence, KV head) to finish: flash-decoding's
-    // log-sum-exp merge of every split's (max, sum, O) of the G query heads
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int* cnt = a.merge_cnt + (size_t)slot * c.Hkv + h;
-        const int last = atomicAdd(cnt, 1) == a.splits - 1;
-        if (last) *cnt = 0;      // every other CTA has counted: ready for the next call
-        last_sh = last;
-    }
-    __syncthreads();
-    if (!last_sh) return;
-    __threadfence();
-    const size_t p0 = ((size_t)b * c.Hkv + h) * a.splits;
-    for (int hh = 0; hh < c.G; ++hh) {
-        float M = NEG_INF;
-        for (int s2 = 0; s2 < a.splits; ++s2) M = fmaxf(M, __ldcg(a.part_ml + ((p0 + s2) * c.G + hh) * 2));
-        float L = 0.f, O = 0.f;
-        if (M != NEG_INF) {
-            for (int s2 = 0; s2 < a.splits; ++s2) {
-                const size_t pi = (p0 + s2) * c.G + hh;
-                const float mm = __ldcg(a.part_ml + pi * 2);
-                if (mm == NEG_INF) continue;
-                const float w = ex2(mm - M);
-                L += w * __ldcg(a.part_ml + pi * 2 + 1);
-                O += w * __ldcg(a.part_o + pi * GD + d);
+    if (a.splits > 1) {
+        // split merge in the last CTA of (sequence, KV head) to finish: flash-decoding's
+        // log-sum-exp merge of every split's (max, sum, O) of the G query heads
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int* cnt = a.merge_cnt + (size_t)slot * c.Hkv + h;
+            const int last = atomicAdd(cnt, 1) == a.splits - 1;
+            if (last) *cnt = 0;      // every other CTA has counted: ready for the next call
+            last_sh = last;
+        }
+        __syncthreads();
+        if (!last_sh) return;
+        __threadfence();
+        // splits folded in index order (this CTA's own from registers), so that the
+        // result does not depend on which CTA finished last
+        const size_t p0 = ((size_t)b * c.Hkv + h) * a.splits;
+        float Mr[8], Lr[8], Or[8];
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) {
+            Mr[hh] = NEG_INF;
+            Lr[hh] = Or[hh] = 0.f;
+        }
+        for (int s2 = 0; s2 < a.splits; ++s2) {
+            // one split's partials of every head, all loads in flight together
+            float ms[8], ls[8], os[8];
+#pragma unroll
+            for (int hh = 0; hh < 8; ++hh) {
+                ms[hh] = Mh[hh];
+                ls[hh] = Lh[hh];
+                os[hh] = Oh[hh];
+                if (hh < c.G && s2 != split) {
+                    const size_t pi = (p0 + s2) * c.G + hh;
+                    ms[hh] = __ldcg(a.part_ml + pi * 2);
+                    ls[hh] = __ldcg(a.part_ml + pi * 2 + 1);
+                    os[hh] = __ldcg(a.part_o + pi * GD + d);
+                }
+            }
+#pragma unroll
+            for (int hh = 0; hh < 8; ++hh) {
+                if (ms[hh] == NEG_INF) continue;
+                const float Mn = fmaxf(Mr[hh], ms[hh]);
+                const float fa = ex2(Mr[hh] - Mn), fb = ex2(ms[hh] - Mn);
+                Lr[hh] = Lr[hh] * fa + ls[hh] * fb;
+                Or[hh] = Or[hh] * fa + os[hh] * fb;
+                Mr[hh] = Mn;
             }
         }
-        a.out[((size_t)b * c.Hq + (size_t)h * c.G + hh) * GD + d] = L > 0.f ? O / L : 0.f;
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) {
+            Lh[hh] = Lr[hh];
+            Oh[hh] = Or[hh];
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < 8; ++hh)
+        if (hh < c.G)
+            a.out[((size_t)b * c.Hq + (size_t)h * c.G + hh) * GD + d] = Lh[hh] > 0.f ? Oh[hh] / Lh[hh] : 0.f;
+    // T advances once per step: counted by the CTA that finishes each (sequence, KV head)
+    // (the merging CTA, or the only split), every CTA of the sequence having read the meta
+    if (a.k_new && threadIdx.x == 0) {
+        if (atomicAdd(&a.meta_rw[slot].pad[0], 1) == (int)gridDim.y - 1) {
+            a.meta_rw[slot].T = m.T;
+            a.meta_rw[slot].pad[0] = 0;
+        }
     }
 }
 

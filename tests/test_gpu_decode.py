@@ -115,6 +115,19 @@ def test_decode_subset_of_slots():
         check_outputs(out[j], oracle.decode_attn(b.ocaches[seq], tok.q[j]), f"subset {seq}")
 
 
+def test_decode_attn_is_bitwise_repeatable():
+    """Splits are merged in a fixed order by whichever CTA finishes last: repeated calls
+    on the same cache give bit-identical outputs (a plan with three or more splits)."""
+    wl = inputs.Workload("rep", 0, 32, 8, 128, 128, 4, 508, 512, 16, 7, 6, 0, 0, 0, 1 / math.sqrt(128))
+    b = Batch(wl, [5000, 3000, 700, 4096, 1200, 2500], slots=list(range(6)), seed=31)
+    assert b.cache.decode_attn_plan(6)[0] >= 3
+    q = inputs.gen_decode(wl, 6, step=0, seed=31).q.cuda()
+    outs = [b.cache.decode_attn(b.dslots, q) for _ in range(5)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
 def test_decode_full_kv_baseline_equals_full_attention():
     """A cache with L_sink = 0, K = 0 and a ring as long as the whole sequence is the
     uncompressed baseline: it must equal attention over every token (torch SDPA)."""
