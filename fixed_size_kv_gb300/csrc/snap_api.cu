@@ -600,6 +600,7 @@ snap_status compress_impl(snap_cache* cache, int slot, const void* K, const void
         if (e != cudaSuccess) return cuda_status(e);
     }
     if (!(stages & SNAP_STAGE_WRITE)) return SNAP_OK;
+    // 5. cache write: every slot
     return cuda_status(launch_cache_write(a, num_sms(), st));
 }
 
