@@ -127,6 +127,8 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
     __shared__ int counts[2];                    // this CTA's (greater, equal) counts
     __shared__ uint32_t sh_prefix;
     __shared__ int sh_kk;
+    __shared__ int sh_done;                      // the descent stopped early
+    __shared__ int peer_counts[SEL_CLUSTER][2];
     const DevConfig& c = a.cfg;
     const int h = blockIdx.y;
     const int rank = (int)cluster.block_rank();
@@ -141,58 +143,88 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
     // this CTA's pooled values: shared memory when they fit, else the workspace
     uint32_t* vals = in_smem ? sel_dyn - i0 : a.pool + (size_t)h * a.S_pad;
 
-    // 0. pooled scores of this slice (the score GEMM leaves each column sum in two halves)
+    // per-warp histogram of one radix digit (shared-memory atomics; lanes that hit the
+    // same bin are serialised by the hardware)
+    auto hist_add = [&](bool match, uint32_t d) {
+        if (match) atomicAdd(&hist_w[warp][d], 1);
+    };
+    for (int i = lane; i < 256; i += 32) hist_w[warp][i] = 0;
+    __syncwarp();
+
+    // 0. pooled scores of this slice (the score GEMM leaves each column sum in two
+    //    halves), with the histogram of their top 8 bits (the first radix pass)
     if (in_smem) {
-        // the column sums of positions L_sink + i0 - rad .. L_sink + i1 - 1 + rad, once
+        // the column sums of positions L_sink + i0 - rad .. L_sink + i1 - 1 + rad, once;
+        // eight positions per thread in flight
         float* raw = reinterpret_cast<float*>(sel_dyn + per);
         const int k0 = c.L_sink + i0 - rad;
         const int nk = (i1 - i0) + 2 * rad;
-        for (int t = tid; t < nk; t += SEL_THREADS) {
-            const int k = k0 + t;
-            raw[t] = (k >= 0 && k < n_sc) ? c0[k] + c1[k] : -__builtin_huge_valf();
+        for (int t0 = 0; t0 < nk; t0 += 8 * SEL_THREADS) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = t0 + e * SEL_THREADS + tid, k = k0 + t;
+                x[e] = (t < nk && k >= 0 && k < n_sc) ? __ldcg(c0 + k) + __ldcg(c1 + k) : -__builtin_huge_valf();
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (t0 + e * SEL_THREADS + tid < nk) raw[t0 + e * SEL_THREADS + tid] = x[e];
         }
         __syncthreads();
-        for (int i = i0 + tid; i < i1; i += SEL_THREADS) {
-            const int t = i - i0 + rad;          // raw index of position L_sink + i
-            float mx = raw[t - rad];
-            for (int d = -rad + 1; d <= rad; ++d) mx = fmaxf(mx, raw[t + d]);
-            vals[i] = __float_as_uint(mx);
+        for (int base = i0; base < i1; base += SEL_THREADS) {
+            const int i = base + tid;
+            const bool in = i < i1;
+            uint32_t v = 0u;
+            if (in) {
+                const int t = i - i0 + rad;          // raw index of position L_sink + i
+                float mx = raw[t - rad];
+                for (int d = -rad + 1; d <= rad; ++d) mx = fmaxf(mx, raw[t + d]);
+                v = __float_as_uint(mx);
+                vals[i] = v;
+            }
+            hist_add(in, v >> 24);
         }
     } else {
-        for (int i = i0 + tid; i < i1; i += SEL_THREADS) {
-            const int j = c.L_sink + i;
-            const int lo = max(0, j - rad), hi = min(n_sc - 1, j + rad);
-            float mx = c0[lo] + c1[lo];
-            for (int k = lo + 1; k <= hi; ++k) mx = fmaxf(mx, c0[k] + c1[k]);
-            vals[i] = __float_as_uint(mx);
+        for (int base = i0; base < i1; base += SEL_THREADS) {
+            const int i = base + tid;
+            const bool in = i < i1;
+            uint32_t v = 0u;
+            if (in) {
+                const int j = c.L_sink + i;
+                const int lo = max(0, j - rad), hi = min(n_sc - 1, j + rad);
+                float mx = c0[lo] + c1[lo];
+                for (int k = lo + 1; k <= hi; ++k) mx = fmaxf(mx, c0[k] + c1[k]);
+                v = __float_as_uint(mx);
+                vals[i] = v;
+            }
+            hist_add(in, v >> 24);
         }
     }
     if (tid == 0) {
         sh_prefix = 0u;
         sh_kk = c.K;
+        sh_done = 0;
     }
     __syncthreads();
 
-    // 1-4. radix descent over the whole middle, 8 bits at a time
+    // 1-4. radix descent over the whole middle, 8 bits at a time.  It stops early when
+    //      the digit's bucket holds exactly the positions still to take: they are all
+    //      kept, so the threshold becomes "at least the bucket's prefix".
     uint32_t mask = 0u;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
         const uint32_t prefix = sh_prefix;
-        for (int i = lane; i < 256; i += 32) hist_w[warp][i] = 0;
-        __syncwarp();
-        for (int base = i0; base < i1; base += SEL_THREADS) {
-            const int i = base + tid;
-            const bool in = i < i1;
-            const uint32_t v = in ? vals[i] : 0u;
-            const bool match = in && (v & mask) == prefix;
-            const unsigned active = __ballot_sync(0xffffffffu, match);
-            if (match) {
-                const int d = (int)((v >> shift) & 255u);
-                const unsigned same = __match_any_sync(active, d);
-                if ((int)(__ffs(same) - 1) == lane) atomicAdd(&hist_w[warp][d], __popc(same));
+        if (pass > 0) {
+            for (int i = lane; i < 256; i += 32) hist_w[warp][i] = 0;
+            __syncwarp();
+            for (int base = i0; base < i1; base += SEL_THREADS) {
+                const int i = base + tid;
+                const bool in = i < i1;
+                const uint32_t v = in ? vals[i] : 0u;
+                hist_add(in && (v & mask) == prefix, (v >> shift) & 255u);
             }
+            __syncthreads();
         }
-        __syncthreads();
         int* hc = hist_cta[pass & 1];
         if (tid < 256) {
             int t = 0;
@@ -217,12 +249,21 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
             d = __shfl_sync(0xffffffffu, d, src);
             kk = __shfl_sync(0xffffffffu, kk, src);
             if (lane == 0) {
-                sh_kk = kk;
-                sh_prefix = prefix | ((uint32_t)d << shift);
+                const uint32_t p = prefix | ((uint32_t)d << shift);
+                if (pass < 3 && kk == hist_all[d] && p != 0u) {
+                    // the whole bucket is kept: keep every value >= p, no ties
+                    sh_prefix = p - 1u;
+                    sh_kk = 0;
+                    sh_done = 1;
+                } else {
+                    sh_kk = kk;
+                    sh_prefix = p;
+                }
             }
         }
         mask |= 255u << shift;
         __syncthreads();
+        if (sh_done) break;
     }
     const uint32_t tau = sh_prefix;
     const int kk = sh_kk;                        // how many scores equal to tau are kept
@@ -236,19 +277,35 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
         gt += v > tau;
         eq += v == tau;
     }
-    int gt_cta, eq_cta;
-    const int gt_before = block_excl_scan(gt, warp_tot, &gt_cta);
-    const int eq_before = block_excl_scan(eq, warp_tot, &eq_cta);
+    int gt_before, eq_before, gt_cta, eq_cta;
+    if (per < 32768) {
+        // one scan of both counts, packed 15 + 16 bits
+        int both_cta;
+        const int both_before = block_excl_scan((gt << 16) | eq, warp_tot, &both_cta);
+        gt_before = both_before >> 16;
+        eq_before = both_before & 0xffff;
+        gt_cta = both_cta >> 16;
+        eq_cta = both_cta & 0xffff;
+    } else {
+        gt_before = block_excl_scan(gt, warp_tot, &gt_cta);
+        eq_before = block_excl_scan(eq, warp_tot, &eq_cta);
+    }
     if (tid == 0) {
         counts[0] = gt_cta;
         counts[1] = eq_cta;
     }
     cluster.sync();
+    // the lower-ranked CTAs' counts, read in parallel
+    if (tid < rank) {
+        const int* cr = cluster.map_shared_rank(counts, tid);
+        peer_counts[tid][0] = cr[0];
+        peer_counts[tid][1] = cr[1];
+    }
+    __syncthreads();
     // positions kept by lower-ranked CTAs, and equal scores met before this slice
     int taken_prev = 0, eq_prev = 0;
     for (int r = 0; r < rank; ++r) {
-        const int* cr = cluster.map_shared_rank(counts, r);
-        const int g = cr[0], e = cr[1];
+        const int g = peer_counts[r][0], e = peer_counts[r][1];
         taken_prev += g + min(max(kk - eq_prev, 0), e);
         eq_prev += e;
     }
