@@ -26,22 +26,34 @@ namespace {
 constexpr float NEG_INF = -__builtin_huge_valf();
 
 // --------------------------------------------------------------------- lse
+// One warp per observation row: the lanes merge the row's key-split partials
+// (max, sum) in parallel, then across the warp.
+__device__ __forceinline__ void ml_merge(float& M, float& L, float m, float l) {
+    const float Mn = fmaxf(M, m);
+    if (Mn == NEG_INF) return;
+    L = L * ex2(M - Mn) + l * ex2(m - Mn);
+    M = Mn;
+}
+
 __global__ void lse_merge_kernel(CompressArgs a) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;   // over Hkv * R_pad
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // over Hkv * R_pad
+    const int lane = threadIdx.x & 31;
     const int total = a.cfg.Hkv * a.R_pad;
     if (i >= total) return;
     const int h = i / a.R_pad, r = i % a.R_pad;
     if (r >= a.R) {
-        a.nlse2[i] = NEG_INF;  // padding rows contribute 2^-inf = 0
+        if (lane == 0) a.nlse2[i] = NEG_INF;  // padding rows contribute 2^-inf = 0
         return;
     }
     const float* p = a.part_ml + ((size_t)h * a.R + r) * a.row_splits * 2;
-    float M = NEG_INF;
-    for (int s = 0; s < a.row_splits; ++s) M = fmaxf(M, p[2 * s]);
-    float L = 0.f;
-    if (M != NEG_INF)
-        for (int s = 0; s < a.row_splits; ++s) L += p[2 * s + 1] * ex2(p[2 * s] - M);
-    a.nlse2[i] = (L > 0.f) ? -(M + log2f(L)) : NEG_INF;
+    float M = NEG_INF, L = 0.f;
+    for (int s = lane; s < a.row_splits; s += 32) ml_merge(M, L, p[2 * s], p[2 * s + 1]);
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) {
+        const float m = __shfl_xor_sync(0xffffffffu, M, x), l = __shfl_xor_sync(0xffffffffu, L, x);
+        ml_merge(M, L, m, l);
+    }
+    if (lane == 0) a.nlse2[i] = (L > 0.f) ? -(M + log2f(L)) : NEG_INF;
 }
 
 // ------------------------------------------------------------------- select
@@ -352,8 +364,8 @@ cudaError_t launch_lse_import(const CompressArgs& a, const float* lse_obs, cudaS
 }
 
 cudaError_t launch_lse_merge(const CompressArgs& a, cudaStream_t st) {
-    const int total = a.cfg.Hkv * a.R_pad;
-    lse_merge_kernel<<<(total + 255) / 256, 256, 0, st>>>(a);
+    const int total = a.cfg.Hkv * a.R_pad;   // rows, one warp each
+    lse_merge_kernel<<<(total + 7) / 8, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 
