@@ -150,8 +150,13 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
     const int rad = c.P / 2;
     const int per = (M + SEL_CLUSTER - 1) / SEL_CLUSTER;
     const int i0 = min(M, rank * per), i1 = min(M, i0 + per);
-    const float* c0 = a.col + (size_t)h * a.S_pad;
-    const float* c1 = a.col + ((size_t)c.Hkv + h) * a.S_pad;
+    // column sum of position k: the score kernel's SCORE_PARTS parts, added in order
+    auto colsum = [&](int k) {
+        float t = __ldcg(a.col + (size_t)h * a.S_pad + k);
+#pragma unroll
+        for (int q = 1; q < SCORE_PARTS; ++q) t += __ldcg(a.col + ((size_t)q * c.Hkv + h) * a.S_pad + k);
+        return t;
+    };
     // this CTA's pooled values: shared memory when they fit, else the workspace
     uint32_t* vals = in_smem ? sel_dyn - i0 : a.pool + (size_t)h * a.S_pad;
 
@@ -176,7 +181,7 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int t = t0 + e * SEL_THREADS + tid, k = k0 + t;
-                x[e] = (t < nk && k >= 0 && k < n_sc) ? __ldcg(c0 + k) + __ldcg(c1 + k) : -__builtin_huge_valf();
+                x[e] = (t < nk && k >= 0 && k < n_sc) ? colsum(k) : -__builtin_huge_valf();
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -204,8 +209,8 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
             if (in) {
                 const int j = c.L_sink + i;
                 const int lo = max(0, j - rad), hi = min(n_sc - 1, j + rad);
-                float mx = c0[lo] + c1[lo];
-                for (int k = lo + 1; k <= hi; ++k) mx = fmaxf(mx, c0[k] + c1[k]);
+                float mx = colsum(lo);
+                for (int k = lo + 1; k <= hi; ++k) mx = fmaxf(mx, colsum(k));
                 v = __float_as_uint(mx);
                 vals[i] = v;
             }

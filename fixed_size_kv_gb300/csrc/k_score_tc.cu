@@ -17,9 +17,10 @@
 //            window row sees, so no causal limit applies).
 //   LOGITS   as ROWSTAT, writing the raw base-2 logits (inspection / GEMM checks).
 //
-// Roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and one thread
-// issues tcgen05.mma, warps 2..9 read TMEM (warp w reads lanes 32*(w%4).., half
-// (w-2)/4 of the columns).  The accumulator is double-buffered in TMEM (2 x 256
+// Roles (576 threads): warp 0 issues TMA loads, warp 1 owns TMEM and one thread
+// issues tcgen05.mma, warps 2..17 read TMEM (warp w reads lanes 32*(w%4).. of part
+// (w-2)/4 of the columns: four epilogue warps per SM sub-partition, so that the
+// latency of one warp's ex2 / add chains is hidden by the others).  The accumulator is double-buffered in TMEM (2 x 256
 // columns) so the epilogue of one tile overlaps the MMAs of the next.  Every wait
 // is bounded; on expiry the kernel records SNAP_ERR_TIMEOUT, drains and exits.
 #include "kernels.cuh"
@@ -36,7 +37,8 @@ enum { ROWSTAT = SCORE_ROWSTAT, COLSUM = SCORE_COLSUM, LOGITS = SCORE_LOGITS };
 constexpr int XROWS = 128;                 // rows of the X operand per MMA (M)
 constexpr int CHUNK_B = 128;               // bytes per swizzled row (64 bf16)
 constexpr int SMEM_BUDGET = 216 * 1024;    // operand bytes per CTA
-constexpr int THREADS = 320;
+constexpr int EPI_WARPS = 4 * SCORE_PARTS;  // epilogue warps: one per (TMEM lane quarter, column part)
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 
 template <int D, bool XRES>
 struct Layout {
@@ -171,7 +173,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_init(bar(B_RES_EMPTY), 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar(B_ACC_FULL + b), 1);
-            mbar_init(bar(B_ACC_EMPTY + b), 8);
+            mbar_init(bar(B_ACC_EMPTY + b), EPI_WARPS);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -272,9 +274,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 2;
         const int quarter = warp & 3;
-        const int half = ew >> 2;
+        const int part = ew >> 2;
         const int trow = quarter * 32 + lane;     // TMEM lane = X row within the tile
-        const int ncol = Ny / 2;                  // columns per half
+        // this part's accumulator columns: Ny / SCORE_PARTS rounded up to whole 32-column
+        // chunks (the last parts get none when Ny is small)
+        const int pcols = ((Ny / SCORE_PARTS + 31) / 32) * 32;
+        const int cbeg = min(Ny, part * pcols);
+        const int ncol = min(Ny, cbeg + pcols) - cbeg;
         const float sl2 = p.sl2;
         uint32_t acc_it = 0;
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
@@ -295,7 +301,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // -lse2 of the observation rows on this tile's columns (same for every lane)
                 const float* nl = (MODE == COLSUM) ? p.nlse2 + (size_t)U.h * p.R_pad + y0 : nullptr;
                 for (int cc = 0; cc < ncol; cc += 32) {
-                    const int col0 = half * ncol + cc;
+                    const int col0 = cbeg + cc;
                     float v[32];
                     tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + buf * 256 + col0, v);
                     tmem_ld_wait();
@@ -355,19 +361,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (MODE == COLSUM) {
                     if (!XRES) {  // a new key tile each step: write its partial column sums
                         const int key = (U.xt0 + s) * XROWS + trow;
-                        if (key < p.n_sc) p.col[((size_t)half * p.Hkv + U.h) * p.S_pad + key] = acc;
+                        if (key < p.n_sc) p.col[((size_t)part * p.Hkv + U.h) * p.S_pad + key] = acc;
                         acc = 0.f;
                     }
                 }
             }
             if (MODE == ROWSTAT && r < p.R) {
-                float* o = p.part_ml + (((size_t)U.h * p.R + r) * (2 * p.splits) + 2 * U.split + half) * 2;
+                float* o = p.part_ml + (((size_t)U.h * p.R + r) * (SCORE_PARTS * p.splits) + SCORE_PARTS * U.split + part) * 2;
                 o[0] = m;
                 o[1] = l;
             }
             if (MODE == COLSUM && XRES && U.nsteps > 0) {
                 const int key = U.xt * XROWS + trow;
-                if (key < p.n_sc) p.col[((size_t)half * p.Hkv + U.h) * p.S_pad + key] = acc;
+                if (key < p.n_sc) p.col[((size_t)part * p.Hkv + U.h) * p.S_pad + key] = acc;
             }
         }
     epi_done:;

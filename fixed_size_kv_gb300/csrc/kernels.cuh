@@ -113,9 +113,9 @@ struct CompressArgs {
     // workspace
     float* part_ml;              // [Hkv][R][row_splits][2]
     float* nlse2;                // [Hkv][R_pad]  -lse2 per observation row (-inf padding)
-    float* col;                  // [2][Hkv][S_pad] column-sum halves (summed by select)
+    float* col;                  // [SCORE_PARTS][Hkv][S_pad] column-sum parts (summed by select)
     uint32_t* pool;              // [Hkv][S_pad] pooled score bits
-    int row_splits;              // partials per row (2 per key split)
+    int row_splits;              // partials per row (SCORE_PARTS per key split)
     int R_pad;
     int64_t S_pad;
     // cache
@@ -142,12 +142,16 @@ struct ScoreParams {
     int R_pad;
     float* part_ml;              // ROWSTAT out: [Hkv][R][2*splits][2]
     const float* nlse2;          // COLSUM in:  [Hkv][R_pad]
-    float* col;                  // COLSUM out: [2][Hkv][S_pad]
+    float* col;                  // COLSUM out: [SCORE_PARTS][Hkv][S_pad]
     int64_t S_pad;
     float* logits;               // LOGITS out: [Hkv][R][S]
     int32_t* status;
 };
 enum { SCORE_ROWSTAT = 0, SCORE_COLSUM = 1, SCORE_LOGITS = 2 };
+// The score kernel's epilogue splits an accumulator's columns into this many parts (four
+// warps each, one per TMEM lane quarter): the row pass leaves SCORE_PARTS partials per
+// row and key split, the column pass SCORE_PARTS column-sum arrays.
+constexpr int SCORE_PARTS = 4;
 cudaError_t launch_score_tc(int mode, const CUtensorMap& tx, const CUtensorMap& ty, const ScoreParams& p,
                             int D, bool x_is_q, bool x_resident, int num_sms, cudaStream_t st);
 cudaError_t launch_cache_write(const CompressArgs& a, int num_sms, cudaStream_t st);

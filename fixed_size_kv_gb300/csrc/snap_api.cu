@@ -28,7 +28,7 @@ struct snap_cache {
 namespace {
 
 constexpr int ABI_VERSION = 1;
-constexpr int MAX_KEY_SPLITS = 32;   // key splits of the row pass (2 partials each)
+constexpr int MAX_KEY_SPLITS = 32;   // key splits of the row pass (SCORE_PARTS partials each)
 constexpr int MAX_DECODE_SPLITS = 32;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -111,11 +111,11 @@ CompressWs compress_ws(const snap_config& c, int64_t S) {
     w.S_pad = (S + 127) / 128 * 128;
     size_t off = 0;
     w.part_ml = off;
-    off = align_up(off + sizeof(float) * 2 * c.n_kv_heads * (size_t)w.R * 2 * MAX_KEY_SPLITS, 256);
+    off = align_up(off + sizeof(float) * 2 * c.n_kv_heads * (size_t)w.R * SCORE_PARTS * MAX_KEY_SPLITS, 256);
     w.nlse2 = off;
     off = align_up(off + sizeof(float) * c.n_kv_heads * (size_t)w.R_pad, 256);
     w.col = off;
-    off = align_up(off + sizeof(float) * 2 * c.n_kv_heads * (size_t)w.S_pad, 256);
+    off = align_up(off + sizeof(float) * SCORE_PARTS * c.n_kv_heads * (size_t)w.S_pad, 256);
     w.pool = off;
     off = align_up(off + sizeof(uint32_t) * c.n_kv_heads * (size_t)w.S_pad, 256);
     w.total = off;
@@ -570,7 +570,7 @@ snap_status compress_impl(snap_cache* cache, int slot, const void* K, const void
             e = run_rowstat(SCORE_ROWSTAT, c, sp, K, S, tok_stride, head_stride, Q_obs, st);
             // 2. merge into -lse2 per row
             if (e == cudaSuccess) {
-                a.row_splits = 2 * row_key_splits(c, w.R, S);
+                a.row_splits = SCORE_PARTS * row_key_splits(c, w.R, S);
                 e = launch_lse_merge(a, st);
             }
         }
