@@ -11,6 +11,8 @@
 // Invalid slots (unused middle slots, ring slots not holding a live position) are
 // masked; whole tiles with no valid slot are not read.  The MLA layout's split merge
 // runs as its own kernel (decode_merge_kernel): 128 heads x 512 values per sequence.
+#include <cooperative_groups.h>
+
 #include "kernels.cuh"
 
 namespace snap {
@@ -291,24 +293,37 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
     }
     __syncthreads();
     const int d = threadIdx.x;  // 128 threads == 128 dims
-    // this CTA's (max, sum, O[d]) per query head, kept for the split merge
+    // this CTA's (max, sum, O[d]) per query head, kept for the split merge: every warp's
+    // values of every head are loaded first, then combined
     float Mh[8], Lh[8], Oh[8];
+    {
+        float wm[G_WARPS][8], wl[G_WARPS][8], wo[G_WARPS][8];
 #pragma unroll
-    for (int hh = 0; hh < 8; ++hh) {
-        Mh[hh] = NEG_INF;
-        Lh[hh] = Oh[hh] = 0.f;
-        if (hh >= c.G) continue;
+        for (int w = 0; w < G_WARPS; ++w)
 #pragma unroll
-        for (int w = 0; w < G_WARPS; ++w) Mh[hh] = fmaxf(Mh[hh], mlb[(w * 8 + hh) * 2]);
-        if (Mh[hh] != NEG_INF) {
+            for (int hh = 0; hh < 8; ++hh) {
+                wm[w][hh] = mlb[(w * 8 + hh) * 2];
+                wl[w][hh] = mlb[(w * 8 + hh) * 2 + 1];
+                wo[w][hh] = ob[(w * 8 + hh) * GD + d];
+            }
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) {
+            Mh[hh] = NEG_INF;
+#pragma unroll
+            for (int w = 0; w < G_WARPS; ++w) Mh[hh] = fmaxf(Mh[hh], wm[w][hh]);
+            Lh[hh] = Oh[hh] = 0.f;
 #pragma unroll
             for (int w = 0; w < G_WARPS; ++w) {
-                const float f = ex2(mlb[(w * 8 + hh) * 2] - Mh[hh]);
-                Lh[hh] += f * mlb[(w * 8 + hh) * 2 + 1];
-                Oh[hh] += f * ob[(w * 8 + hh) * GD + d];
+                const float f = Mh[hh] == NEG_INF ? 0.f : ex2(wm[w][hh] - Mh[hh]);
+                Lh[hh] += f * wl[w][hh];
+                Oh[hh] += f * wo[w][hh];
             }
         }
-        if (a.splits > 1) {
+    }
+    if (a.splits > 1 && !a.cluster_merge) {
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) {
+            if (hh >= c.G) continue;
             const size_t pi = (((size_t)b * c.Hkv + h) * a.splits + split) * c.G + hh;
             a.part_o[pi * GD + d] = Oh[hh];
             if (d == 0) {
@@ -317,7 +332,60 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
             }
         }
     }
-    if (a.splits > 1) {
+    if (a.splits > 1 && a.cluster_merge) {
+        // the splits of this (sequence, KV head) are one cluster (rank = split).  Once
+        // every rank's loop is done, each writes its (max, sum, O) into rank 0's pipeline
+        // buffers (free by then) through distributed shared memory; after the second
+        // barrier rank 0 folds them in rank order from its own shared memory.
+        namespace cg = cooperative_groups;
+        cg::cluster_group cl = cg::this_cluster();
+        constexpr int ML_OFF = 8 * 8 * GD;        // [rank][8 heads][GD] O, then [rank][8][2]
+        static_assert((ML_OFF + 8 * 8 * 2) * 4 <= G_SMEM, "landing area inside the pipeline buffers");
+        cl.sync();
+        float* land = cl.map_shared_rank(reinterpret_cast<float*>(smem), 0);
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh)
+            if (hh < c.G) {
+                land[(split * 8 + hh) * GD + d] = Oh[hh];
+                if (d == 0) {
+                    land[ML_OFF + (split * 8 + hh) * 2 + 0] = Mh[hh];
+                    land[ML_OFF + (split * 8 + hh) * 2 + 1] = Lh[hh];
+                }
+            }
+        cl.sync();
+        if (split != 0) return;
+        const float* xo = reinterpret_cast<const float*>(smem);
+        float Mr[8], Lr[8], Or[8];
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) {
+            Mr[hh] = NEG_INF;
+            Lr[hh] = Or[hh] = 0.f;
+        }
+        for (int s2 = 0; s2 < a.splits; ++s2) {
+            // a rank's values of every head loaded first (slots of heads >= G are unused)
+            float ms[8], ls[8], os[8];
+#pragma unroll
+            for (int hh = 0; hh < 8; ++hh) {
+                ms[hh] = xo[ML_OFF + (s2 * 8 + hh) * 2];
+                ls[hh] = xo[ML_OFF + (s2 * 8 + hh) * 2 + 1];
+                os[hh] = xo[(s2 * 8 + hh) * GD + d];
+            }
+#pragma unroll
+            for (int hh = 0; hh < 8; ++hh) {
+                if (hh >= c.G || ms[hh] == NEG_INF) continue;
+                const float Mn = fmaxf(Mr[hh], ms[hh]);
+                const float fa = ex2(Mr[hh] - Mn), fb = ex2(ms[hh] - Mn);
+                Lr[hh] = Lr[hh] * fa + ls[hh] * fb;
+                Or[hh] = Or[hh] * fa + os[hh] * fb;
+                Mr[hh] = Mn;
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) {
+            Lh[hh] = Lr[hh];
+            Oh[hh] = Or[hh];
+        }
+    } else if (a.splits > 1) {
         // split merge in the last CTA of (sequence, KV head) to finish: flash-decoding's
         // log-sum-exp merge of every split's (max, sum, O) of the G query heads
         __threadfence();
@@ -440,11 +508,53 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
 
 }  // namespace
 
-cudaError_t launch_decode_gqa(const DecodeArgs& a, cudaStream_t st) {
+// Clusters of `csize` decode CTAs that can be resident at once on this device (0 if
+// the query fails); cached per device and cluster size.
+int gqa_active_clusters(int csize) {
+    static std::atomic<int> cached[64][9];     // zero-initialised (static storage)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const bool cacheable = dev >= 0 && dev < 64 && csize >= 0 && csize <= 8;
+    if (cacheable) {
+        const int v = cached[dev][csize].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(csize, 1, 1);
+    cfg.blockDim = dim3(G_WARPS * 32);
+    cfg.dynamicSmemBytes = G_SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = csize;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gqa_decode_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (cacheable && n > 0) cached[dev][csize].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+cudaError_t launch_decode_gqa(const DecodeArgs& a0, cudaStream_t st) {
     static std::atomic<uint64_t> smem_set{0};
     if (cudaError_t e = opt_in_smem(gqa_decode_kernel, G_SMEM, smem_set); e != cudaSuccess) return e;
-    dim3 grid(a.splits, a.cfg.Hkv, a.n);
-    return launch_dependent(gqa_decode_kernel, grid, dim3(G_WARPS * 32), G_SMEM, st, a);
+    dim3 grid(a0.splits, a0.cfg.Hkv, a0.n);
+    // the splits of a (sequence, KV head) as one cluster when a portable cluster holds
+    // them and every cluster of the launch is resident at once (else the global merge)
+    if (a0.splits >= 2 && a0.splits <= 8) {
+        const long long ctas = (long long)a0.splits * a0.cfg.Hkv * a0.n;
+        if (ctas <= (long long)gqa_active_clusters(a0.splits) * a0.splits) {
+            DecodeArgs a = a0;
+            a.cluster_merge = 1;
+            return launch_dependent_clustered(gqa_decode_kernel, grid, dim3(G_WARPS * 32), G_SMEM, st,
+                                              (unsigned)a.splits, a);
+        }
+    }
+    return launch_dependent(gqa_decode_kernel, grid, dim3(G_WARPS * 32), G_SMEM, st, a0);
 }
 
 cudaError_t launch_decode_merge(const DecodeArgs& a, cudaStream_t st) {

@@ -35,6 +35,9 @@ struct DecodeArgs {
     const bf16* v_new;           // [n][Hkv][dv] (GQA)
     snap_seq_meta* meta_rw;      // the same meta, writable (append only)
     int32_t* merge_cnt;          // [max_batch][Hkv] CTAs of (slot, head) done; zero between calls
+    // GQA: the splits of one (sequence, KV head) run as one thread-block cluster and
+    // merge through distributed shared memory (set by the launch when 2..8 splits)
+    int cluster_merge;
 };
 
 constexpr int GQA_KEYS = 32;     // keys per warp step of the GQA decode kernel
@@ -56,6 +59,27 @@ cudaError_t launch_dependent(void (*kernel)(Exp...), dim3 grid, dim3 block, size
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
+}
+
+// As launch_dependent, with clusters of cluster_x CTAs along the grid's x.
+template <typename... Exp, typename... Act>
+cudaError_t launch_dependent_clustered(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                       unsigned cluster_x, Act&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = cluster_x;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Act&&>(args)...);
 }
 
