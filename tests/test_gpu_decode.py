@@ -128,6 +128,18 @@ def test_decode_attn_is_bitwise_repeatable():
         assert torch.equal(o, outs[0])
 
 
+def test_decode_splits_beyond_a_cluster():
+    """One sequence on a 32768-slot cache: the plan has more than eight splits, so the
+    splits merge through the global partials (the last CTA to finish folds them), not
+    within a cluster.  Fused steps against the oracle."""
+    wl = inputs.Workload("wide", 0, 32, 8, 128, 128, 4, 16380, 16384, 16, 7, 1, 0, 0, 0, 1 / math.sqrt(128))
+    b = Batch(wl, [20000], [0], seed=37)
+    assert b.cache.decode_attn_plan(1)[0] > 8
+    for t in range(4):
+        b.step(t, fused=True)
+    b.check_rows()
+
+
 def test_decode_full_kv_baseline_equals_full_attention():
     """A cache with L_sink = 0, K = 0 and a ring as long as the whole sequence is the
     uncompressed baseline: it must equal attention over every token (torch SDPA)."""
