@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 METRIC = "decode tok/s + HBM GB/s (fixed cache vs full KV) at 128k ctx; compress ms"
 L2_BYTES = 129 << 20
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0      # the ~8 TB/s nominal HBM3e figure decode is also reported against
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
@@ -194,6 +195,16 @@ def window_lse(wl, K, Q):
     return out.contiguous()
 
 
+def algorithmic_decode_flop(wl, metas):
+    """FLOP one decode-attention launch must do: per valid cache row and query head, the
+    score (2 d_qk) and the weighted value sum (2 d_v)."""
+    valid = 0
+    for m in metas:
+        S, T, R0, n_sink, n_mid = m
+        valid += n_sink + n_mid + min(T - R0, wl.L_recent)
+    return valid * wl.G * 2.0 * (wl.d_qk + wl.d_v) * wl.n_kv_heads
+
+
 def algorithmic_decode_bytes(wl, metas):
     """Bytes one decode-attention launch must move: every valid cache row once
     (keys, plus values for GQA), the queries and the outputs."""
@@ -329,6 +340,7 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
     mid_metas = [(S, S + D // 2, R0, ns, nm) for (S, T, R0, ns, nm) in
                  [(m[0], m[1], m[2], m[3], m[4]) for m in metas]]
     attn_bytes = algorithmic_decode_bytes(wl, mid_metas)
+    attn_flop = algorithmic_decode_flop(wl, mid_metas)
 
     # working set of one step: prompts, cache, decode inputs and outputs
     work_bytes = sum(p.K.numel() * 2 + (p.V.numel() * 2 if p.V is not None else 0) for p in pre)
@@ -525,6 +537,9 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
                            "note": "snap_compress per sequence against one GEMM's FLOP"},
             "whole_call_with_prefill_lse": {"ms": cmp_lse_ms, "achieved": tf(cmp_lse_ms),
                                             "frac": tf(cmp_lse_ms) / bf16_burst},
+            # on the FLOP the MMAs issue: two passes without the prefill's LSE, one with it
+            "issued": {"whole_call": {"flop": 2 * F, "frac": 2 * tf(cmp_ms / B) / bf16_burst},
+                       "whole_call_with_prefill_lse": {"flop": F, "frac": tf(cmp_lse_ms) / bf16_burst}},
         }
     cache_write_bytes = statistics.mean(2 * wl.n_kv_heads * wl.C * (wl.d_qk + (wl.d_v if wl.layout == 0 else 0)) * 2
                                         for _ in lengths)
@@ -549,7 +564,15 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
             "compress_with_prefill_lse_ms_per_seq": cmp_lse_ms,
             "compress_stage_ms_per_seq": stage_ms,
             "attn": {"ms": attn_avg_ms, "hbm_gbs": attn_gbs, "bytes_per_launch": attn_bytes,
-                     "frac": attn_gbs / hbm_peak, "eager_launch_ms": eager_launch_ms,
+                     "frac": attn_gbs / hbm_peak, "frac_of_nominal": attn_gbs / NOMINAL_HBM_GBS,
+                     "nominal_gbs": NOMINAL_HBM_GBS,
+                     # the same launch against the tensor roofline (bf16 sustained: the decode
+                     # loop runs for a long time); it matters for the MLA layout, at the ridge
+                     "tensor": {"flop_per_launch": attn_flop,
+                                "achieved_tflops": attn_flop / (attn_avg_ms / 1e3) / 1e12,
+                                "peak": bf16_sus,
+                                "frac": attn_flop / (attn_avg_ms / 1e3) / 1e12 / bf16_sus},
+                     "eager_launch_ms": eager_launch_ms,
                      "timing": ("graph-replayed decode loop / steps" if graph is not None
                                 else "CUDA events around each eager launch")},
             "full_kv": full,
