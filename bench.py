@@ -729,7 +729,8 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
     back, all inside the timed region.  The copies run on a second stream into two sets
     of device buffers: step i+1's inputs upload while step i computes (the first step's
     upload is not hidden), and within a step each compression waits for its own prompt
-    only.  The outputs of a step's decode steps come back in one copy at its end."""
+    only.  The outputs of a step's decode steps come back in one copy on the copy stream,
+    overlapping the next step; the timed region ends when the last step's are on the host."""
     import torch
     from fixed_size_kv_gb300 import snap
     B, D = wl.batch, wl.decode_steps
@@ -738,7 +739,6 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
     hQ = [p.Q.to("cpu").pin_memory() for p in pre]
     hq, hk = q_all.to("cpu").pin_memory(), k_all.to("cpu").pin_memory()
     hv = v_all.to("cpu").pin_memory() if v_all is not None else None
-    hout = torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.float32).pin_memory()
 
     def buffers():
         return {"K": [torch.empty_like(p.K) for p in pre],
@@ -746,16 +746,17 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
                 "Q": [torch.empty_like(p.Q) for p in pre],
                 "q": torch.empty_like(q_all), "k": torch.empty_like(k_all),
                 "v": torch.empty_like(v_all) if v_all is not None else None,
+                "out": torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev),
+                "hout": torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.float32).pin_memory(),
                 "up": [torch.cuda.Event() for _ in range(B)], "up_dec": torch.cuda.Event(),
-                "done": torch.cuda.Event(), "used": False}
+                "done": torch.cuda.Event(), "read": torch.cuda.Event(), "used": False, "read_pending": False}
 
     sets = [buffers(), buffers()]
-    dout = torch.empty((D, B, wl.n_q_heads, wl.d_v), dtype=torch.float32, device=dev)
     cache = snap.SnapCache(cfg, max_batch=B, max_prompt=max(lengths), max_n=B, device=dev, stream=stream)
     slots = torch.arange(B, dtype=torch.int32, device=dev)
     h2d = sum(x.numel() * 2 for x in hK + hQ) + sum(x.numel() * 2 for x in hV if x is not None)
     h2d += (q_all.numel() + k_all.numel() + (v_all.numel() if v_all is not None else 0)) * 2
-    d2h = dout.numel() * 4
+    d2h = D * B * wl.n_q_heads * wl.d_v * 4
     copy = torch.cuda.Stream(device=dev)
 
     def upload(st):
@@ -776,16 +777,22 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
             st["up_dec"].record(copy)
 
     def compute(st):
+        if st["read_pending"]:
+            stream.wait_event(st["read"])   # this set's previous outputs are on the host
         for b in range(B):
             stream.wait_event(st["up"][b])
             cache.compress(b, st["K"][b], st["V"][b], st["Q"][b], stream=stream)
         stream.wait_event(st["up_dec"])
         for t in range(D):
             cache.decode_step(slots, st["q"][t], st["k"][t], st["v"][t] if st["v"] is not None else None,
-                              out=dout[t], stream=stream)
-        with torch.cuda.stream(stream):
-            hout.copy_(dout, non_blocking=True)
+                              out=st["out"][t], stream=stream)
         st["done"].record(stream)
+        # the step's outputs go back on the copy stream, overlapping the next step
+        copy.wait_event(st["done"])
+        with torch.cuda.stream(copy):
+            st["hout"].copy_(st["out"], non_blocking=True)
+        st["read"].record(copy)
+        st["read_pending"] = True
 
     # untimed warm-up of both buffer sets
     for w in range(2):
@@ -796,7 +803,8 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
     # this host's pinned host->device bandwidth, on one prompt (explains the e2e number)
     c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     c0.record(copy)
-    sets[0]["K"][0].copy_(hK[0], non_blocking=True)
+    with torch.cuda.stream(copy):
+        sets[0]["K"][0].copy_(hK[0], non_blocking=True)
     c1.record(copy)
     copy.synchronize()
     h2d_gbs = hK[0].numel() * 2 / (c0.elapsed_time(c1) / 1e3) / 1e9
@@ -809,6 +817,7 @@ def run_e2e(args, wl, lengths, pre, q_all, k_all, v_all, cfg, dev, stream, world
         if i + 1 < steps:
             upload(sets[(i + 1) % 2])
         compute(sets[i % 2])
+    stream.wait_stream(copy)                # the last step's outputs are on the host
     e1.record(stream)
     stream.synchronize()
     ms = reduce_max(e0.elapsed_time(e1))
