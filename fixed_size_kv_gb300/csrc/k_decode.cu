@@ -4,10 +4,12 @@
 // memory-bound, so the cache bytes streamed per step set the time per token.
 // GQA: each CTA streams one contiguous range of cache slots of one (sequence, KV head)
 // once from HBM and produces an un-normalised partial (max, sum, O) per query head;
-// the last CTA of a (sequence, KV head) to finish combines the splits (flash-decoding's
-// log-sum-exp merge), so a decode step is one launch.  The ring append of the step
-// ("Ring Buffer vs. Naive Slicing": scatter the new token into its fixed ring slot) is
-// fused in: the CTA whose key range holds the slot writes the new row before reading.
+// the splits are combined by flash-decoding's log-sum-exp merge inside the same launch:
+// within a thread-block cluster (2-8 splits, through distributed shared memory) or by
+// the last CTA of the (sequence, KV head) to finish (through global memory), so a decode
+// step is one launch.  The ring append of the step ("Ring Buffer vs. Naive Slicing":
+// scatter the new token into its fixed ring slot) is fused in: the warp whose tile holds
+// the slot writes the new row to the cache and into its own copy of the tile.
 // Invalid slots (unused middle slots, ring slots not holding a live position) are
 // masked; whole tiles with no valid slot are not read.  The MLA layout's split merge
 // runs as its own kernel (decode_merge_kernel): 128 heads x 512 values per sequence.
