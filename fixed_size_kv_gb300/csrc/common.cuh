@@ -146,6 +146,21 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+// max of three floats in one instruction (-inf is the identity; a NaN operand is ignored
+// unless all are NaN, as for fmaxf)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float m;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+    return m;
+}
+// acc (two fp32 lanes) += (lo, hi), one packed add
+__device__ __forceinline__ void add_f32x2(uint64_t& acc, uint32_t lo, uint32_t hi) {
+    asm("{\n .reg .b64 t;\n mov.b64 t, {%1, %2};\n add.rn.f32x2 %0, %0, t;\n}\n" : "+l"(acc) : "r"(lo), "r"(hi));
+}
+// the sum of a packed pair's two fp32 lanes
+__device__ __forceinline__ float f32x2_sum(uint64_t x) {
+    return __uint_as_float((uint32_t)x) + __uint_as_float((uint32_t)(x >> 32));
+}
 __device__ __forceinline__ float bf16_round(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));
 }

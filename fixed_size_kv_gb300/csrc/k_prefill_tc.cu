@@ -247,11 +247,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int e = 0; e < 32; ++e)
                         if (key0 + c * 32 + e > row) v[c][e] = NEG_INF;
             }
-            float mx = NEG_INF;
+            // the row max: eight independent chains, three operands per instruction
+            float mq[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int k = 0; k < 8; ++k) mq[k] = fmaxf(v[0][2 * k], v[0][2 * k + 1]);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) mx = fmaxf(mx, v[c][e]);
+            for (int i = 16; i < 128; i += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mq[k] = fmax3(mq[k], v[(i + 2 * k) >> 5][(i + 2 * k) & 31], v[(i + 2 * k + 1) >> 5][(i + 2 * k + 1) & 31]);
+            float mx = fmax3(fmax3(mq[0], mq[1], mq[2]), fmax3(mq[3], mq[4], mq[5]), fmaxf(mq[6], mq[7]));
             mx *= sl2;                                   // sl2 > 0: the max of the scaled scores
             // lazy running max; O is rescaled (warp-wide, tcgen05 is warp-collective) when
             // a lane's max moves and its old max was finite, after P V of the last tile
@@ -290,25 +295,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                 float (&hi)[32] = v[2 * c2 + 1];
                 float w[32];
                 const float nm = -m_used;
-                float sb[4] = {0.f, 0.f, 0.f, 0.f}, se[4] = {0.f, 0.f, 0.f, 0.f};
+                // sums of the bf16 weights (and, for the log-sum-exp rows, of the unrounded
+                // ones) as packed f32x2 accumulators, two weights per add
+                uint64_t sb2[2] = {0ull, 0ull}, se2[2] = {0ull, 0ull};
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const float p0 = ex2(fmaf(lo[2 * e], sl2, nm)), p1 = ex2(fmaf(lo[2 * e + 1], sl2, nm));
                     const uint32_t pk = pack_bf16(p0, p1);   // the weights P V uses
-                    sb[e & 3] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xffff0000u);
-                    if (need_lse) se[e & 3] += p0 + p1;
+                    add_f32x2(sb2[e & 1], pk << 16, pk & 0xffff0000u);
+                    if (need_lse) add_f32x2(se2[e & 1], __float_as_uint(p0), __float_as_uint(p1));
                     w[e] = __uint_as_float(pk);
                 }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const float p0 = ex2(fmaf(hi[2 * e], sl2, nm)), p1 = ex2(fmaf(hi[2 * e + 1], sl2, nm));
                     const uint32_t pk = pack_bf16(p0, p1);
-                    sb[e & 3] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xffff0000u);
-                    if (need_lse) se[e & 3] += p0 + p1;
+                    add_f32x2(sb2[e & 1], pk << 16, pk & 0xffff0000u);
+                    if (need_lse) add_f32x2(se2[e & 1], __float_as_uint(p0), __float_as_uint(p1));
                     w[16 + e] = __uint_as_float(pk);
                 }
-                l_bf += (sb[0] + sb[1]) + (sb[2] + sb[3]);
-                l_ex += (se[0] + se[1]) + (se[2] + se[3]);
+                l_bf += f32x2_sum(sb2[0]) + f32x2_sum(sb2[1]);
+                l_ex += f32x2_sum(se2[0]) + f32x2_sum(se2[1]);
                 tmem_st32(tS + c2 * 32, w);
             }
             tmem_st_wait();
