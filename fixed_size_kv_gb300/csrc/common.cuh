@@ -157,6 +157,17 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 __device__ __forceinline__ void add_f32x2(uint64_t& acc, uint32_t lo, uint32_t hi) {
     asm("{\n .reg .b64 t;\n mov.b64 t, {%1, %2};\n add.rn.f32x2 %0, %0, t;\n}\n" : "+l"(acc) : "r"(lo), "r"(hi));
 }
+// (a0, a1) = (x0, x1) * m + b, lane by lane, one packed fma (m, b: packed pairs)
+__device__ __forceinline__ void fma_f32x2(float& a0, float& a1, float x0, float x1, uint64_t m, uint64_t b) {
+    asm("{\n .reg .b64 x, y;\n mov.b64 x, {%2, %3};\n fma.rn.f32x2 y, x, %4, %5;\n mov.b64 {%0, %1}, y;\n}\n"
+        : "=f"(a0), "=f"(a1)
+        : "f"(x0), "f"(x1), "l"(m), "l"(b));
+}
+// both lanes of a packed pair set to x
+__device__ __forceinline__ uint64_t f32x2_splat(float x) {
+    const uint64_t u = __float_as_uint(x);
+    return u | (u << 32);
+}
 // the sum of a packed pair's two fp32 lanes
 __device__ __forceinline__ float f32x2_sum(uint64_t x) {
     return __uint_as_float((uint32_t)x) + __uint_as_float((uint32_t)(x >> 32));

@@ -298,9 +298,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // sums of the bf16 weights (and, for the log-sum-exp rows, of the unrounded
                 // ones) as packed f32x2 accumulators, two weights per add
                 uint64_t sb2[2] = {0ull, 0ull}, se2[2] = {0ull, 0ull};
+                const uint64_t sl2x2 = f32x2_splat(sl2), nmx2 = f32x2_splat(nm);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2(fmaf(lo[2 * e], sl2, nm)), p1 = ex2(fmaf(lo[2 * e + 1], sl2, nm));
+                    float a0, a1;
+                    fma_f32x2(a0, a1, lo[2 * e], lo[2 * e + 1], sl2x2, nmx2);
+                    const float p0 = ex2(a0), p1 = ex2(a1);
                     const uint32_t pk = pack_bf16(p0, p1);   // the weights P V uses
                     add_f32x2(sb2[e & 1], pk << 16, pk & 0xffff0000u);
                     if (need_lse) add_f32x2(se2[e & 1], __float_as_uint(p0), __float_as_uint(p1));
@@ -308,7 +311,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float p0 = ex2(fmaf(hi[2 * e], sl2, nm)), p1 = ex2(fmaf(hi[2 * e + 1], sl2, nm));
+                    float a0, a1;
+                    fma_f32x2(a0, a1, hi[2 * e], hi[2 * e + 1], sl2x2, nmx2);
+                    const float p0 = ex2(a0), p1 = ex2(a1);
                     const uint32_t pk = pack_bf16(p0, p1);
                     add_f32x2(sb2[e & 1], pk << 16, pk & 0xffff0000u);
                     if (need_lse) add_f32x2(se2[e & 1], __float_as_uint(p0), __float_as_uint(p1));
