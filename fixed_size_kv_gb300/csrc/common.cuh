@@ -163,6 +163,10 @@ __device__ __forceinline__ void fma_f32x2(float& a0, float& a1, float x0, float 
         : "=f"(a0), "=f"(a1)
         : "f"(x0), "f"(x1), "l"(m), "l"(b));
 }
+// the packed pair (lo, hi)
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
+}
 // both lanes of a packed pair set to x
 __device__ __forceinline__ uint64_t f32x2_splat(float x) {
     const uint64_t u = __float_as_uint(x);

@@ -58,25 +58,32 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
     return mbar_wait_bounded(bar, parity, abort_flag);
 }
 
-// sum_i 2^(v_i * a + b) over 32 values, with independent partial sums
+// sum_i 2^(v_i * a + b) over 32 values: the arguments two at a time (packed f32x2 FMA),
+// the sums in four packed f32x2 accumulators
 __device__ __forceinline__ float sum32_ex2(const float (&v)[32], float a, float b) {
-    float t[8];
+    const uint64_t a2 = f32x2_splat(a), b2 = f32x2_splat(b);
+    uint64_t t[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t[k] = ex2(fmaf(v[k], a, b));
-#pragma unroll
-    for (int i = 8; i < 32; i += 8)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) t[k] += ex2(fmaf(v[i + k], a, b));
-    return ((t[0] + t[1]) + (t[2] + t[3])) + ((t[4] + t[5]) + (t[6] + t[7]));
+    for (int k = 0; k < 16; ++k) {
+        float x0, x1;
+        fma_f32x2(x0, x1, v[2 * k], v[2 * k + 1], a2, b2);
+        add_f32x2(t[k & 3], __float_as_uint(ex2(x0)), __float_as_uint(ex2(x1)));
+    }
+    return (f32x2_sum(t[0]) + f32x2_sum(t[1])) + (f32x2_sum(t[2]) + f32x2_sum(t[3]));
 }
 
+// max of 32 values: four chains of three-operand max
 __device__ __forceinline__ float max32(const float (&v)[32]) {
-    float t[8];
+    float t[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t[k] = fmaxf(v[k], v[k + 8]);
+    for (int k = 0; k < 4; ++k) t[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);   // 0..11
 #pragma unroll
-    for (int k = 0; k < 8; ++k) t[k] = fmaxf(t[k], fmaxf(v[k + 16], v[k + 24]));
-    return fmaxf(fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3])), fmaxf(fmaxf(t[4], t[5]), fmaxf(t[6], t[7])));
+    for (int i = 12; i < 28; i += 8)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[k] = fmax3(t[k], v[i + 2 * k], v[i + 2 * k + 1]);   // 12..27
+#pragma unroll
+    for (int k = 0; k < 4; ++k) t[k] = fmaxf(t[k], v[28 + k]);                           // 28..31
+    return fmaxf(fmaxf(t[0], t[1]), fmaxf(t[2], t[3]));
 }
 
 struct Unit {
@@ -336,16 +343,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                         l += sum;
                     } else if (MODE == COLSUM) {
                         const float4* nl4 = reinterpret_cast<const float4*>(nl + col0);
-                        float s4[4] = {0.f, 0.f, 0.f, 0.f};   // independent accumulators
+                        const uint64_t sl2x2 = f32x2_splat(sl2);
+                        uint64_t s2[2] = {0ull, 0ull};   // packed f32x2 accumulators
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float4 b = __ldg(nl4 + i);
-                            s4[0] += ex2(fmaf(v[4 * i + 0], sl2, b.x));
-                            s4[1] += ex2(fmaf(v[4 * i + 1], sl2, b.y));
-                            s4[2] += ex2(fmaf(v[4 * i + 2], sl2, b.z));
-                            s4[3] += ex2(fmaf(v[4 * i + 3], sl2, b.w));
+                            float x0, x1, x2, x3;
+                            fma_f32x2(x0, x1, v[4 * i + 0], v[4 * i + 1], sl2x2, f32x2_pack(b.x, b.y));
+                            fma_f32x2(x2, x3, v[4 * i + 2], v[4 * i + 3], sl2x2, f32x2_pack(b.z, b.w));
+                            add_f32x2(s2[0], __float_as_uint(ex2(x0)), __float_as_uint(ex2(x1)));
+                            add_f32x2(s2[1], __float_as_uint(ex2(x2)), __float_as_uint(ex2(x3)));
                         }
-                        acc += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                        acc += f32x2_sum(s2[0]) + f32x2_sum(s2[1]);
                     } else {  // LOGITS
                         if (r < p.R) {
                             float* o = p.logits + ((size_t)U.h * p.R + r) * p.S;
