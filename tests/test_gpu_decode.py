@@ -128,6 +128,22 @@ def test_decode_attn_is_bitwise_repeatable():
         assert torch.equal(o, outs[0])
 
 
+def test_decode_eight_split_cluster():
+    """Two sequences on a 4096-slot cache: the plan has 5-8 splits, so each (sequence, KV
+    head) is one cluster of that many CTAs merging through distributed shared memory.
+    Fused steps against the oracle; repeated calls bitwise equal."""
+    wl = inputs.Workload("c8", 0, 32, 8, 128, 128, 4, 2044, 2048, 16, 7, 2, 0, 0, 0, 1 / math.sqrt(128))
+    b = Batch(wl, [6000, 3500], [0, 1], seed=41)
+    assert 5 <= b.cache.decode_attn_plan(2)[0] <= 8
+    for t in range(3):
+        b.step(t, fused=True)
+    q = inputs.gen_decode(wl, 2, step=9, seed=41).q.cuda()
+    outs = [b.cache.decode_attn(b.dslots, q) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert all(torch.equal(o, outs[0]) for o in outs[1:])
+    b.check_rows()
+
+
 def test_decode_splits_beyond_a_cluster():
     """One sequence on a 32768-slot cache: the plan has more than eight splits, so the
     splits merge through the global partials (the last CTA to finish folds them), not
