@@ -16,8 +16,8 @@
 //   S_t = Q_t K_j^T    M = 128 rows, N = 128 keys, 8 MMAs over d (A, B in shared memory)
 //   O_t += P_t V_j     M = 128 rows, N = 128 (d), 8 MMAs over keys (P in TMEM, V MN-major)
 // TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 each; P_t (bf16) is written over S_t.
-// Roles (320 threads): warp 0 TMA, warp 1 TMEM + MMA issue, warps 2..5 softmax of
-// tile 0, warps 6..9 softmax of tile 1 (thread = query row).  The running max moves
+// Roles (384 threads, three warpgroups): warp 0 TMA, warp 1 TMEM + MMA issue (warps 2, 3
+// idle), warps 4..7 softmax of tile 0, warps 8..11 softmax of tile 1 (thread = query row).  The running max moves
 // lazily (only when a tile's max exceeds it by more than 8 in log2 units; O is then
 // rescaled in TMEM), so most tiles skip the rescale.  P is rounded to bf16 for the
 // MMA and the output's normaliser sums those rounded weights; the log-sum-exp sums the
@@ -34,7 +34,14 @@ constexpr int D = 128;                        // head dim
 constexpr int BM = 128;                       // query rows per tile
 constexpr int BN = 128;                       // keys per tile
 constexpr int CHB = 128 * 128;                // one 64-column chunk of a 128-row tile: 16 KB
-constexpr int THREADS = 320;
+constexpr int THREADS = 384;                  // three warpgroups
+// Registers: the launch gives 168 per thread (384 threads); the load / MMA warpgroup
+// gives back all but SETUP_REGS and each softmax warpgroup takes SOFTMAX_REGS, within
+// the launch's total (80 * 128 + 208 * 256 = 63,488 <= 168 * 384 = 64,512), so the
+// softmax keeps a tile's 128 scores in registers without spilling.
+constexpr int SETUP_REGS = 80;
+constexpr int SOFTMAX_REGS = 208;
+static_assert(SETUP_REGS * 128 + SOFTMAX_REGS * 256 <= 168 * THREADS, "register split within the launch's");
 constexpr float RESCALE_GAP = 8.f;
 
 constexpr int OFF_Q = 0;                      // 2 tiles x 2 chunks
@@ -105,6 +112,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         report_error(a.status, SNAP_ERR_TIMEOUT, 500, role, cur);
     };
 
+    // warpgroup 0 (warps 0-3: TMA, MMA, two idle) hands registers to the two softmax
+    // warpgroups (warps 4-7, 8-11)
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(SETUP_REGS));
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -208,9 +219,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_commit(bar(B_KV_EMPTY + st));    // after both P V of key tile j
             }
         }
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(SOFTMAX_REGS));
         // ------------------------------------------------------------ softmax groups
-        const int t = (warp - 2) >> 2;                   // query tile of this group
+        const int t = (warp - 4) >> 2;                   // query tile of this group
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;               // row within the tile (TMEM lane)
         const int qt = qt0 + t;
