@@ -146,6 +146,19 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+// L2 policy for data that the next kernel reads again: its lines are evicted after
+// those of streaming traffic (evict_last, on the whole access).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Global store of one float with an L2 policy.
+__device__ __forceinline__ void st_global_policy(float* ptr, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(pol) : "memory");
+}
+
 // max of three floats in one instruction (-inf is the identity; a NaN operand is ignored
 // unless all are NaN, as for fmaxf)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {

@@ -205,6 +205,7 @@ __global__ void __launch_bounds__(CB_WARPS * 32) cache_write_kernel(CompressArgs
     __shared__ int abort_flag;
     const DevConfig& c = a.cfg;
     if (threadIdx.x == 0) abort_flag = 0;
+    pdl_wait();                 // the selection (and everything before it) is complete and visible
     __syncthreads();
     const int warp = threadIdx.x >> 5;
     const int64_t n_warps = (int64_t)gridDim.x * CB_WARPS, w = (int64_t)blockIdx.x * CB_WARPS + warp;
@@ -247,8 +248,7 @@ cudaError_t launch_cache_write(const CompressArgs& a, int num_sms, cudaStream_t 
     long long blocks = (batches + CB_WARPS - 1) / CB_WARPS;
     if (blocks > num_sms) blocks = num_sms;
     if (blocks < a.cfg.Hkv) blocks = a.cfg.Hkv;
-    cache_write_kernel<<<(unsigned)blocks, CB_WARPS * 32, CW_SMEM, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(cache_write_kernel, dim3((unsigned)blocks), dim3(CB_WARPS * 32), CW_SMEM, st, a);
 }
 
 }  // namespace snap

@@ -36,6 +36,8 @@ __device__ __forceinline__ void ml_merge(float& M, float& L, float m, float l) {
 }
 
 __global__ void lse_merge_kernel(CompressArgs a) {
+    pdl_wait();                 // the row pass's partials are complete and visible
+    pdl_launch_dependents();    // the column pass may launch (it waits for this grid)
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // over Hkv * R_pad
     const int lane = threadIdx.x & 31;
     const int total = a.cfg.Hkv * a.R_pad;
@@ -57,7 +59,8 @@ __global__ void lse_merge_kernel(CompressArgs a) {
 }
 
 // ------------------------------------------------------------------- select
-// One cluster of SEL_CLUSTER CTAs per KV head; CTA r owns a contiguous slice of
+// One cluster of CL CTAs per KV head (16 or 12 where the device can hold every head's
+// cluster at once, else 8); CTA r owns a contiguous slice of
 // the middle positions.  The slice's column sums (plus the pooling halo) are read
 // once into shared memory and max-pooled there; the pooled scores (non-negative
 // floats, compared as their IEEE bit patterns, which order them) stay in shared
@@ -68,35 +71,19 @@ __global__ void lse_merge_kernel(CompressArgs a) {
 // and, among the scores equal to it, the lowest positions.
 constexpr int SEL_THREADS = 1024;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
-constexpr int SEL_CLUSTER = 8;
 
-// Exclusive prefix sum over the block; *total receives the block sum.
-__device__ __forceinline__ int block_excl_scan(int x, int* warp_tot, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// In-place exclusive prefix sum of v[0..31] by one warp; returns the total.
+__device__ __forceinline__ int warp_excl_scan32(int* v) {
+    const int lane = threadIdx.x & 31;
+    const int x = v[lane];
     int incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o) incl += y;
     }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const int v = warp_tot[lane];
-        int vi = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, vi, o);
-            if (lane >= o) vi += y;
-        }
-        warp_tot[lane] = vi - v;
-        if (lane == 31) warp_tot[32] = vi;
-    }
-    __syncthreads();
-    const int r = warp_tot[warp] + incl - x;
-    *total = warp_tot[32];
-    __syncthreads();
-    return r;
+    v[lane] = incl - x;
+    return __shfl_sync(0xffffffffu, incl, 31);
 }
 
 // Digit of this radix pass that holds the kk-th largest value: the largest d with
@@ -127,20 +114,46 @@ __device__ __forceinline__ void find_digit(const int* hist, int kk, int* digit, 
     }
 }
 
-__global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREADS, 1)
-    select_kernel(CompressArgs a, int in_smem) {
+// Max-pool of four consecutive positions with radius RAD <= 4: w[m] holds the raw sum of
+// the position 4 - m places before the first output.
+template <int RAD>
+__device__ __forceinline__ void pool4(const float (&w)[12], float (&o)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float mx = w[4 + j - RAD];
+#pragma unroll
+        for (int d = -RAD + 1; d <= RAD; ++d) mx = fmaxf(mx, w[4 + j + d]);
+        o[j] = mx;
+    }
+}
+
+// Raw column sums held per side of a select CTA's slice: the pooling radius, at least 4
+// so that the four-position path reads whole 16-byte groups.
+__host__ __device__ __forceinline__ int select_pad(int P) { return P / 2 > 4 ? P / 2 : 4; }
+// Raw column sums read for a slice of n positions: with the four-position path (radius
+// <= 4) whole groups of four plus the two groups its last loads reach, else the slice
+// and its halo.
+__host__ __device__ __forceinline__ int select_raw_words(int n, int P) {
+    return P / 2 <= 4 ? 4 * ((n + 3) / 4) + 12 : n + 2 * select_pad(P);
+}
+
+template <int CL>
+__global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a, int in_smem) {
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
-    extern __shared__ uint32_t sel_dyn[];         // [per] pooled bits, then [per + 2 rad] raw sums
+    extern __shared__ uint4 sel_dyn4[];           // [per] pooled bits, then [per + 2 pad] raw sums
+    uint32_t* sel_dyn = reinterpret_cast<uint32_t*>(sel_dyn4);
     __shared__ int hist_w[SEL_WARPS][256];       // per-warp private histograms
     __shared__ int hist_cta[2][256];             // this CTA's histogram, double-buffered by pass
     __shared__ int hist_all[256];
-    __shared__ int warp_tot[33];
+    __shared__ int warp_gt[SEL_WARPS], warp_eq[SEL_WARPS];   // per-warp counts, then their scans
     __shared__ int counts[2];                    // this CTA's (greater, equal) counts
     __shared__ uint32_t sh_prefix;
     __shared__ int sh_kk;
     __shared__ int sh_done;                      // the descent stopped early
-    __shared__ int peer_counts[SEL_CLUSTER][2];
+    __shared__ int peer_counts[CL][2];
+    pdl_wait();                 // the column sums are complete and visible
+    pdl_launch_dependents();    // the cache write may launch (it waits for this grid)
     const DevConfig& c = a.cfg;
     const int h = blockIdx.y;
     const int rank = (int)cluster.block_rank();
@@ -148,7 +161,7 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
     const int n_sc = a.S - c.W;
     const int M = a.R0 - c.L_sink;               // middle candidates [L_sink, R0)
     const int rad = c.P / 2;
-    const int per = (M + SEL_CLUSTER - 1) / SEL_CLUSTER;
+    const int per = (M + CL - 1) / CL;
     const int i0 = min(M, rank * per), i1 = min(M, i0 + per);
     // column sum of position k: the score kernel's SCORE_PARTS parts, added in order
     auto colsum = [&](int k) {
@@ -168,14 +181,15 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
     for (int i = lane; i < 256; i += 32) hist_w[warp][i] = 0;
     __syncwarp();
 
-    // 0. pooled scores of this slice (the score GEMM leaves each column sum in two
-    //    halves), with the histogram of their top 8 bits (the first radix pass)
+    // 0. pooled scores of this slice, with the histogram of their top 8 bits (the first
+    //    radix pass)
     if (in_smem) {
-        // the column sums of positions L_sink + i0 - rad .. L_sink + i1 - 1 + rad, once;
-        // eight positions per thread in flight
-        float* raw = reinterpret_cast<float*>(sel_dyn + per);
-        const int k0 = c.L_sink + i0 - rad;
-        const int nk = (i1 - i0) + 2 * rad;
+        // the column sums of positions L_sink + i0 - pad .. (at least L_sink + i1 - 1 +
+        // pad), once (outside the scored range: -inf); eight positions per thread in flight
+        const int pad = select_pad(c.P);
+        float* raw = reinterpret_cast<float*>(sel_dyn + ((per + 3) & ~3));   // 16-byte aligned
+        const int k0 = c.L_sink + i0 - pad;
+        const int nk = select_raw_words(i1 - i0, c.P);
         for (int t0 = 0; t0 < nk; t0 += 8 * SEL_THREADS) {
             float x[8];
 #pragma unroll
@@ -188,18 +202,48 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
                 if (t0 + e * SEL_THREADS + tid < nk) raw[t0 + e * SEL_THREADS + tid] = x[e];
         }
         __syncthreads();
-        for (int base = i0; base < i1; base += SEL_THREADS) {
-            const int i = base + tid;
-            const bool in = i < i1;
-            uint32_t v = 0u;
-            if (in) {
-                const int t = i - i0 + rad;          // raw index of position L_sink + i
-                float mx = raw[t - rad];
-                for (int d = -rad + 1; d <= rad; ++d) mx = fmaxf(mx, raw[t + d]);
-                v = __float_as_uint(mx);
-                vals[i] = v;
+        if (rad <= 4) {
+            // four consecutive positions per thread from three 16-byte loads
+            const float4* raw4 = reinterpret_cast<const float4*>(raw);
+            uint4* out4 = reinterpret_cast<uint4*>(sel_dyn);                  // position i0 + 4q.. at q
+            const int nq = (i1 - i0 + 3) / 4;
+            for (int qb = 0; qb < nq; qb += SEL_THREADS) {
+                const int q = qb + tid;
+                float o[4] = {0.f, 0.f, 0.f, 0.f};
+                if (q < nq) {
+                    const float4 A = raw4[q], B = raw4[q + 1], C = raw4[q + 2];
+                    const float w[12] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w, C.x, C.y, C.z, C.w};
+                    switch (rad) {
+                        case 0: pool4<0>(w, o); break;
+                        case 1: pool4<1>(w, o); break;
+                        case 2: pool4<2>(w, o); break;
+                        case 3: pool4<3>(w, o); break;
+                        default: pool4<4>(w, o); break;
+                    }
+                    // positions past the slice keep 0 (never read as candidates)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (i0 + 4 * q + j >= i1) o[j] = 0.f;
+                    out4[q] = make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                                         __float_as_uint(o[3]));
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) hist_add(q < nq && i0 + 4 * q + j < i1, __float_as_uint(o[j]) >> 24);
             }
-            hist_add(in, v >> 24);
+        } else {
+            for (int base = i0; base < i1; base += SEL_THREADS) {
+                const int i = base + tid;
+                const bool in = i < i1;
+                uint32_t v = 0u;
+                if (in) {
+                    const int t = i - i0 + pad;          // raw index of position L_sink + i
+                    float mx = raw[t - rad];
+                    for (int d = -rad + 1; d <= rad; ++d) mx = fmaxf(mx, raw[t + d]);
+                    v = __float_as_uint(mx);
+                    vals[i] = v;
+                }
+                hist_add(in, v >> 24);
+            }
         }
     } else {
         for (int base = i0; base < i1; base += SEL_THREADS) {
@@ -253,7 +297,7 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
         if (tid < 256) {
             int t = 0;
 #pragma unroll
-            for (int r = 0; r < SEL_CLUSTER; ++r) t += cluster.map_shared_rank(hc, r)[tid];
+            for (int r = 0; r < CL; ++r) t += cluster.map_shared_rank(hc, r)[tid];
             hist_all[tid] = t;
         }
         __syncthreads();
@@ -285,31 +329,31 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
     const uint32_t tau = sh_prefix;
     const int kk = sh_kk;                        // how many scores equal to tau are kept
 
-    // 5. ordered compaction: thread t scans a contiguous run of this slice
-    const int run = (i1 - i0 + SEL_THREADS - 1) / SEL_THREADS;
-    const int r0 = min(i1, i0 + tid * run), r1 = min(i1, r0 + run);
+    // 5. ordered compaction: warp w takes a contiguous block of the slice (whole groups
+    //    of 32 positions), its lanes reading consecutive positions; ballots order the
+    //    kept positions within each group
+    const int wrun = ((i1 - i0 + SEL_WARPS * 32 - 1) / (SEL_WARPS * 32)) * 32;
+    const int w0 = min(i1, i0 + warp * wrun), w1 = min(i1, w0 + wrun);
     int gt = 0, eq = 0;
-    for (int i = r0; i < r1; ++i) {
+    for (int i = w0 + lane; i < w1; i += 32) {
         const uint32_t v = vals[i];
         gt += v > tau;
         eq += v == tau;
     }
-    int gt_before, eq_before, gt_cta, eq_cta;
-    if (per < 32768) {
-        // one scan of both counts, packed 15 + 16 bits
-        int both_cta;
-        const int both_before = block_excl_scan((gt << 16) | eq, warp_tot, &both_cta);
-        gt_before = both_before >> 16;
-        eq_before = both_before & 0xffff;
-        gt_cta = both_cta >> 16;
-        eq_cta = both_cta & 0xffff;
-    } else {
-        gt_before = block_excl_scan(gt, warp_tot, &gt_cta);
-        eq_before = block_excl_scan(eq, warp_tot, &eq_cta);
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
+    if (lane == 0) {
+        warp_gt[warp] = gt;
+        warp_eq[warp] = eq;
     }
-    if (tid == 0) {
-        counts[0] = gt_cta;
-        counts[1] = eq_cta;
+    __syncthreads();
+    if (warp == 0) {
+        const int gt_cta = warp_excl_scan32(warp_gt);
+        const int eq_cta = warp_excl_scan32(warp_eq);
+        if (lane == 0) {
+            counts[0] = gt_cta;
+            counts[1] = eq_cta;
+        }
     }
     cluster.sync();
     // the lower-ranked CTAs' counts, read in parallel
@@ -327,19 +371,22 @@ __global__ void __cluster_dims__(SEL_CLUSTER, 1, 1) __launch_bounds__(SEL_THREAD
         eq_prev += e;
     }
     int32_t* out = a.sel + ((size_t)a.slot * c.Hkv + h) * c.K;
-    // this thread's first output index: greater ones before it in the slice, plus the
-    // equal ones before it that are kept
-    const int eq_g = eq_prev + eq_before;       // equal scores before this thread's run
-    int pos = taken_prev + gt_before + min(max(kk - eq_prev, 0), eq_before);
-    int e_seen = eq_g;
-    for (int i = r0; i < r1; ++i) {
-        const uint32_t v = vals[i];
-        bool take = v > tau;
-        if (v == tau) {
-            take = e_seen < kk;
-            ++e_seen;
-        }
-        if (take) out[pos++] = c.L_sink + i;
+    // this warp's first output index: greater ones before its block, plus the equal
+    // ones before it that are kept
+    const int eq_before = warp_eq[warp];
+    int pos = taken_prev + warp_gt[warp] + min(max(kk - eq_prev, 0), eq_before);
+    int e_seen = eq_prev + eq_before;           // equal scores before the current group
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const uint32_t v = (i < w1) ? vals[i] : 0u;
+        const bool ise = i < w1 && v == tau;
+        const unsigned be = __ballot_sync(0xffffffffu, ise);
+        const bool take = (i < w1 && v > tau) || (ise && e_seen + __popc(be & lt) < kk);
+        const unsigned bt = __ballot_sync(0xffffffffu, take);
+        if (take) out[pos + __popc(bt & lt)] = c.L_sink + i;
+        pos += __popc(bt);
+        e_seen += __popc(be);
     }
     cluster.sync();                              // peers may still read this CTA's counters
 }
@@ -350,6 +397,7 @@ namespace {
 // Row r = w*G + g of KV head h is query head h*G + g at window position w; the
 // caller's LSE is natural-log: -lse2 = -lse * log2(e).
 __global__ void lse_import_kernel(CompressArgs a, const float* lse_obs) {
+    pdl_launch_dependents();    // the column pass may launch (it waits for this grid)
     const int i = blockIdx.x * blockDim.x + threadIdx.x;   // over Hkv * R_pad
     if (i >= a.cfg.Hkv * a.R_pad) return;
     const int h = i / a.R_pad, r = i % a.R_pad;
@@ -370,23 +418,89 @@ cudaError_t launch_lse_import(const CompressArgs& a, const float* lse_obs, cudaS
 
 cudaError_t launch_lse_merge(const CompressArgs& a, cudaStream_t st) {
     const int total = a.cfg.Hkv * a.R_pad;   // rows, one warp each
-    lse_merge_kernel<<<(total + 7) / 8, 256, 0, st>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(lse_merge_kernel, dim3((total + 7) / 8), dim3(256), 0, st, a);
 }
 
-cudaError_t launch_select(const CompressArgs& a, cudaStream_t st) {
-    // pooled values (and the raw column sums they come from) of one CTA's slice in
-    // shared memory when they fit next to the histograms, else in the workspace
-    constexpr int DYN_MAX = 150 * 1024;
-    static std::atomic<uint64_t> smem_set{0};
+namespace {
+constexpr int SEL_DYN_MAX = 150 * 1024;
+
+// Dynamic shared memory of one select CTA holding its slice (pooled values and the
+// raw column sums with the pooling halo); 0 when the slice goes to the workspace.
+long long select_slice_bytes(const CompressArgs& a, int cl) {
     const int M = a.R0 - a.cfg.L_sink;
-    const int per = (M + SEL_CLUSTER - 1) / SEL_CLUSTER;
-    const long long bytes = 4ll * (2ll * per + 2 * (a.cfg.P / 2));
-    const int in_smem = bytes <= DYN_MAX;
-    if (cudaError_t e = opt_in_smem(select_kernel, DYN_MAX, smem_set); e != cudaSuccess) return e;
-    dim3 grid(SEL_CLUSTER, a.cfg.Hkv);
-    select_kernel<<<grid, SEL_THREADS, in_smem ? (size_t)bytes : 0, st>>>(a, in_smem);
-    return cudaGetLastError();
+    const int per = (M + cl - 1) / cl;
+    const long long bytes = 4ll * (((per + 3) & ~3) + (long long)select_raw_words(per, a.cfg.P));
+    return bytes <= SEL_DYN_MAX ? bytes : 0;
+}
+
+// Clusters of CL select CTAs that can be resident at once on this device (0 if the
+// device refuses that size); the kernel's attributes are set on the way.  Cached per
+// device.
+template <int CL>
+int select_active_clusters() {
+    static std::atomic<int> cached[64];        // zero-initialised; -1 = refused
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const bool cacheable = dev >= 0 && dev < 64;
+    if (cacheable) {
+        const int v = cached[dev].load(std::memory_order_relaxed);
+        if (v != 0) return v > 0 ? v : 0;
+    }
+    int n = 0;
+    if ((CL <= 8 || cudaFuncSetAttribute(select_kernel<CL>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                        cudaSuccess) &&
+        cudaFuncSetAttribute(select_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize, SEL_DYN_MAX) ==
+            cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(CL, 1, 1);
+        cfg.blockDim = dim3(SEL_THREADS);
+        cfg.dynamicSmemBytes = SEL_DYN_MAX;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = CL;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, select_kernel<CL>, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();                          // a refusal above is an answer, not an error
+    if (cacheable) cached[dev].store(n > 0 ? n : -1, std::memory_order_relaxed);
+    return n;
+}
+
+template <int CL>
+cudaError_t launch_select_cl(const CompressArgs& a, cudaStream_t st) {
+    const long long bytes = select_slice_bytes(a, CL);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL, a.cfg.Hkv, 1);
+    cfg.blockDim = dim3(SEL_THREADS);
+    cfg.dynamicSmemBytes = (size_t)bytes;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = CL;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    // the kernel waits for the previous grid before its first read
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, select_kernel<CL>, a, bytes > 0 ? 1 : 0);
+}
+}  // namespace
+
+cudaError_t launch_select(const CompressArgs& a, cudaStream_t st) {
+    // the largest cluster (shortest slices) with every head's cluster resident at once
+    // (a cluster stays within one GPC); the portable 8 otherwise
+    if (a.cfg.Hkv <= select_active_clusters<16>()) return launch_select_cl<16>(a, st);
+    if (a.cfg.Hkv <= select_active_clusters<12>()) return launch_select_cl<12>(a, st);
+    if (select_active_clusters<8>() == 0) {
+        static std::atomic<uint64_t> smem_set{0};
+        if (cudaError_t e = opt_in_smem(select_kernel<8>, SEL_DYN_MAX, smem_set); e != cudaSuccess) return e;
+    }
+    return launch_select_cl<8>(a, st);
 }
 
 }  // namespace snap

@@ -196,6 +196,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // the next kernel (the selection after a column pass) may launch and wait for this grid
+    pdl_launch_dependents();
 
     auto fail = [&](int role, int u) {
         *abort_flag = 1;
@@ -279,6 +281,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // launched behind the row statistics' merge (column pass): -lse2 is read from here
+        // on; the loads and MMAs above read only the caller's K and Q
+        pdl_wait();
         const int ew = warp - 2;
         const int quarter = warp & 3;
         const int part = ew >> 2;
@@ -289,6 +294,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int cbeg = min(Ny, part * pcols);
         const int ncol = min(Ny, cbeg + pcols) - cbeg;
         const float sl2 = p.sl2;
+        // COLSUM: the column sums stay in L2 for the selection that reads them next,
+        // past the key tiles streaming through it
+        const uint64_t keep_l2 = l2_policy_evict_last();
         uint32_t acc_it = 0;
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
             const Unit U = decode_unit<MODE, XRES>(u, p);
@@ -370,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (MODE == COLSUM) {
                     if (!XRES) {  // a new key tile each step: write its partial column sums
                         const int key = (U.xt0 + s) * XROWS + trow;
-                        if (key < p.n_sc) p.col[((size_t)part * p.Hkv + U.h) * p.S_pad + key] = acc;
+                        if (key < p.n_sc) st_global_policy(p.col + ((size_t)part * p.Hkv + U.h) * p.S_pad + key, acc, keep_l2);
                         acc = 0.f;
                     }
                 }
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (MODE == COLSUM && XRES && U.nsteps > 0) {
                 const int key = U.xt * XROWS + trow;
-                if (key < p.n_sc) p.col[((size_t)part * p.Hkv + U.h) * p.S_pad + key] = acc;
+                if (key < p.n_sc) st_global_policy(p.col + ((size_t)part * p.Hkv + U.h) * p.S_pad + key, acc, keep_l2);
             }
         }
     epi_done:;
@@ -396,7 +404,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int MODE, int D, bool XQ, bool XRES>
-cudaError_t launch_inst(const CUtensorMap& tx, const CUtensorMap& ty, const ScoreParams& p, int num_sms,
+cudaError_t launch_inst(const CUtensorMap& tx, const CUtensorMap& ty, const ScoreParams& p, int num_sms, bool pdl,
                         cudaStream_t st) {
     using L = Layout<D, XRES>;
     static std::atomic<uint64_t> smem_set{0};
@@ -404,6 +412,7 @@ cudaError_t launch_inst(const CUtensorMap& tx, const CUtensorMap& ty, const Scor
         return e;
     const int grid = p.n_units < num_sms ? p.n_units : num_sms;
     if (grid <= 0) return cudaSuccess;
+    if (pdl) return launch_dependent(score_tc_kernel<MODE, D, XQ, XRES>, dim3(grid), dim3(THREADS), L::TOTAL, st, tx, ty, p);
     score_tc_kernel<MODE, D, XQ, XRES><<<grid, THREADS, L::TOTAL, st>>>(tx, ty, p);
     return cudaGetLastError();
 }
@@ -411,21 +420,21 @@ cudaError_t launch_inst(const CUtensorMap& tx, const CUtensorMap& ty, const Scor
 }  // namespace
 
 cudaError_t launch_score_tc(int mode, const CUtensorMap& tx, const CUtensorMap& ty, const ScoreParams& p,
-                            int D, bool x_is_q, bool x_resident, int num_sms, cudaStream_t st) {
+                            int D, bool x_is_q, bool x_resident, int num_sms, bool pdl, cudaStream_t st) {
     if (mode == ROWSTAT && D == 128 && x_is_q && x_resident)
-        return launch_inst<ROWSTAT, 128, true, true>(tx, ty, p, num_sms, st);
+        return launch_inst<ROWSTAT, 128, true, true>(tx, ty, p, num_sms, pdl, st);
     if (mode == ROWSTAT && D == 576 && x_is_q && x_resident)
-        return launch_inst<ROWSTAT, 576, true, true>(tx, ty, p, num_sms, st);
+        return launch_inst<ROWSTAT, 576, true, true>(tx, ty, p, num_sms, pdl, st);
     if (mode == LOGITS && D == 128 && x_is_q && x_resident)
-        return launch_inst<LOGITS, 128, true, true>(tx, ty, p, num_sms, st);
+        return launch_inst<LOGITS, 128, true, true>(tx, ty, p, num_sms, pdl, st);
     if (mode == LOGITS && D == 576 && x_is_q && x_resident)
-        return launch_inst<LOGITS, 576, true, true>(tx, ty, p, num_sms, st);
+        return launch_inst<LOGITS, 576, true, true>(tx, ty, p, num_sms, pdl, st);
     if (mode == COLSUM && D == 128 && !x_is_q && !x_resident)
-        return launch_inst<COLSUM, 128, false, false>(tx, ty, p, num_sms, st);
+        return launch_inst<COLSUM, 128, false, false>(tx, ty, p, num_sms, pdl, st);
     if (mode == COLSUM && D == 128 && !x_is_q && x_resident)
-        return launch_inst<COLSUM, 128, false, true>(tx, ty, p, num_sms, st);
+        return launch_inst<COLSUM, 128, false, true>(tx, ty, p, num_sms, pdl, st);
     if (mode == COLSUM && D == 576 && !x_is_q && x_resident)
-        return launch_inst<COLSUM, 576, false, true>(tx, ty, p, num_sms, st);
+        return launch_inst<COLSUM, 576, false, true>(tx, ty, p, num_sms, pdl, st);
     return cudaErrorInvalidValue;
 }
 

@@ -177,7 +177,7 @@ enum { SCORE_ROWSTAT = 0, SCORE_COLSUM = 1, SCORE_LOGITS = 2 };
 // row and key split, the column pass SCORE_PARTS column-sum arrays.
 constexpr int SCORE_PARTS = 4;
 cudaError_t launch_score_tc(int mode, const CUtensorMap& tx, const CUtensorMap& ty, const ScoreParams& p,
-                            int D, bool x_is_q, bool x_resident, int num_sms, cudaStream_t st);
+                            int D, bool x_is_q, bool x_resident, int num_sms, bool pdl, cudaStream_t st);
 cudaError_t launch_cache_write(const CompressArgs& a, int num_sms, cudaStream_t st);
 
 // ------------------------------------------- causal prefill attention (tcgen05 + TMA)

@@ -219,7 +219,7 @@ cudaError_t run_rowstat(int mode, const snap_config& c, ScoreParams sp, const vo
     sp.x_tiles = (sp.R + 127) / 128;
     sp.splits = row_key_splits(c, sp.R, S);
     sp.n_units = c.n_kv_heads * sp.x_tiles * sp.splits;
-    return launch_score_tc(mode, tx, ty, sp, c.d_qk, true, true, num_sms(), st);
+    return launch_score_tc(mode, tx, ty, sp, c.d_qk, true, true, num_sms(), false, st);
 }
 
 // MLA decode tensor map of the cache rows [max_batch][C][576] (box 64 x 64).
@@ -593,7 +593,10 @@ snap_status compress_impl(snap_cache* cache, int slot, const void* K, const void
                 sp.splits = 1;
                 sp.n_units = c.n_kv_heads * nx;
             }
-            e = launch_score_tc(SCORE_COLSUM, tx, ty, sp, c.d_qk, false, !y_resident, num_sms(), st);
+            // behind this call's own row stage (a normal launch first) the pass may launch
+            // early: it reads the caller's K and Q, complete before that stage started
+            e = launch_score_tc(SCORE_COLSUM, tx, ty, sp, c.d_qk, false, !y_resident, num_sms(),
+                                (stages & SNAP_STAGE_ROWS) != 0, st);
         }
         // 4. pool + top-K
         if (e == cudaSuccess && (stages & SNAP_STAGE_SELECT)) e = launch_select(a, st);
