@@ -231,6 +231,16 @@ def score_pass_flop(wl, lengths):
     return statistics.mean(2.0 * wl.G * wl.W * wl.d_qk * S * wl.n_kv_heads for S in lengths)
 
 
+def compress_hbm_bytes(wl, lengths, passes):
+    """Algorithmic HBM bytes of one compression call per sequence (mean over the batch):
+    each score pass reads the prompt's keys once (S x Hkv x d_qk bf16) and the cache write
+    reads and writes the kept rows (C x Hkv rows of d_qk + d_v bf16, MLA's one 576-wide
+    row); the window queries and the column sums (a few MB) are left out."""
+    row = wl.d_qk + (wl.d_v if wl.layout == 0 else 0)
+    return statistics.mean(passes * 2.0 * S * wl.n_kv_heads * wl.d_qk + 2 * 2.0 * wl.n_kv_heads * wl.C * row
+                           for S in lengths)
+
+
 def gpu_head_start(stream, ms=1.0):
     """Enqueues about `ms` of device-side sleep on `stream`, so that the host has queued
     the launches that follow (and their events) before the GPU reaches them: the events
@@ -541,6 +551,20 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
             "issued": {"whole_call": {"flop": 2 * F, "frac": 2 * tf(cmp_ms / B) / bf16_burst},
                        "whole_call_with_prefill_lse": {"flop": F, "frac": tf(cmp_lse_ms) / bf16_burst}},
         }
+
+        def call_roofline(ms, passes):
+            hb = compress_hbm_bytes(wl, lengths, passes)
+            t_hbm = hb / (hbm_peak * 1e9) * 1e3              # ms at the measured copy peak
+            t_tc = passes * F / (bf16_burst * 1e12) * 1e3    # ms at the measured bf16 burst
+            floor = max(t_hbm, t_tc)
+            return {"ms": ms, "hbm_bytes": hb, "flop": passes * F, "hbm_floor_ms": t_hbm,
+                    "tensor_floor_ms": t_tc, "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                    "achieved_gbs": hb / (ms / 1e3) / 1e9, "frac": floor / ms}
+        # the whole call against its own floor: the larger of its bytes at the HBM peak and
+        # its GEMM FLOP at the bf16 burst (frac = floor / measured time)
+        compress_roofline["call"] = {"with_prefill_lse": call_roofline(cmp_lse_ms, 1),
+                                     "both_passes": call_roofline(cmp_ms / B, 2),
+                                     "hbm_peak_gbs": hbm_peak, "bf16_peak_tflops": bf16_burst}
     cache_write_bytes = statistics.mean(2 * wl.n_kv_heads * wl.C * (wl.d_qk + (wl.d_v if wl.layout == 0 else 0)) * 2
                                         for _ in lengths)
 
