@@ -93,6 +93,28 @@ def test_compress_edge_cases(case):
     check_all(wl, pre, cache, ocache, where=str(case))
 
 
+@pytest.mark.parametrize("case", [
+    dict(S=3000, n_q_heads=32, n_kv_heads=16),   # more heads than 12-CTA select clusters fit at once
+    dict(S=3001, P=9),                           # pooling radius 4: the widest four-position path
+    dict(S=2999, P=11),                          # pooling radius 5: one position per thread
+])
+def test_compress_select_paths(case):
+    """The select kernel's cluster sizes and pooling paths, each against the oracle."""
+    case = dict(case)
+    S = case.pop("S")
+    wl = small_gqa(**case)
+    pre, cache, ocache = run_compress(wl, S, seed=S)
+    check_all(wl, pre, cache, ocache, where=str(case))
+
+
+def test_compress_select_slices_in_workspace():
+    """A 400k-token prompt on one KV head: each select CTA's slice outgrows shared memory, so
+    the pooled scores go through the workspace."""
+    wl = small_gqa(n_q_heads=2, n_kv_heads=1, W=4, K=5000, L_recent=1024)
+    pre, cache, ocache = run_compress(wl, 400_000, seed=11)
+    check_all(wl, pre, cache, ocache, where="400k one head")
+
+
 def test_compress_group_of_eight_and_strided_inputs():
     """G = 8 query heads per KV head; K and V passed as strided views."""
     wl = small_gqa(n_q_heads=16, n_kv_heads=2, W=8)
