@@ -458,8 +458,10 @@ __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs 
 // =================================================================== merge
 // out[b][i][:] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s  (zero if empty).
 // Partial index: ((b * Hkv + h) * splits + s) * G + hh  for query head i = h*G + hh.
-// One warp turns the (max, sum) pairs into weights in shared memory once; every
-// output column then reads its splits with independent loads.
+// Every thread first requests its columns of the first MERGE_PRE splits (they do not
+// depend on the weights), then one warp turns the (max, sum) pairs into weights in
+// shared memory; the splits are added in index order.
+constexpr int MERGE_PRE = 8;
 __global__ void decode_merge_kernel(DecodeArgs a) {
     pdl_wait();                 // the attention's partials are complete and visible
     __shared__ float w_s[32];
@@ -470,6 +472,15 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
     const int slot = a.slots[b];
     const bool ok = slot >= 0 && slot < c.max_batch;
     const size_t p0 = ((size_t)b * c.Hkv + h) * a.splits;
+    const int dv4 = c.dv / 4;
+    auto part = [&](int s, int d4) {
+        return reinterpret_cast<const float4*>(a.part_o + ((p0 + s) * c.G + hh) * c.dv)[d4];
+    };
+    // this thread's first column group: its loads overlap the weights below
+    float4 pre[MERGE_PRE];
+#pragma unroll
+    for (int s = 0; s < MERGE_PRE; ++s)
+        pre[s] = (ok && s < a.splits && (int)threadIdx.x < dv4) ? part(s, threadIdx.x) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (threadIdx.x < 32) {
         const int s = threadIdx.x;
         const bool in = ok && s < a.splits;
@@ -487,15 +498,27 @@ __global__ void decode_merge_kernel(DecodeArgs a) {
     }
     __syncthreads();
     const float il = inv_l;
-    // four output columns per thread (d_v is 128 or 512): every split's load of a
-    // thread is in flight at once
-    const int dv4 = c.dv / 4;
+    // four output columns per thread (d_v is 128 or 512)
     for (int d4 = threadIdx.x; d4 < dv4; d4 += blockDim.x) {
         float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
         if (il != 0.f) {
+            int s0 = 0;
+            if (d4 == (int)threadIdx.x) {     // the prefetched splits
+#pragma unroll
+                for (int s = 0; s < MERGE_PRE; ++s) {
+                    if (s < a.splits) {
+                        const float w = w_s[s];
+                        O.x += w * pre[s].x;
+                        O.y += w * pre[s].y;
+                        O.z += w * pre[s].z;
+                        O.w += w * pre[s].w;
+                    }
+                }
+                s0 = a.splits < MERGE_PRE ? a.splits : MERGE_PRE;
+            }
 #pragma unroll 8
-            for (int s = 0; s < a.splits; ++s) {
-                const float4 v = reinterpret_cast<const float4*>(a.part_o + ((p0 + s) * c.G + hh) * c.dv)[d4];
+            for (int s = s0; s < a.splits; ++s) {
+                const float4 v = part(s, d4);
                 const float w = w_s[s];
                 O.x += w * v.x;
                 O.y += w * v.y;
