@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a, 
     __shared__ uint32_t sh_prefix;
     __shared__ int sh_kk;
     __shared__ int sh_done;                      // the descent stopped early
+    __shared__ int sh_digit;                     // the digit picked by the last pass
     __shared__ int peer_counts[CL][2];
     pdl_wait();                 // the column sums are complete and visible
     pdl_launch_dependents();    // the cache write may launch (it waits for this grid)
@@ -172,6 +173,13 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a, 
     };
     // this CTA's pooled values: shared memory when they fit, else the workspace
     uint32_t* vals = in_smem ? sel_dyn - i0 : a.pool + (size_t)h * a.S_pad;
+    // warp w owns positions [w0, w1) of the slice (whole groups of four, the pooling's
+    // quads), its lanes taking consecutive positions: every loop over positions uses this
+    // split, so a warp's histograms count exactly the block it compacts
+    const int nq_all = (i1 - i0 + 3) / 4;
+    const int nqw = (nq_all + SEL_WARPS - 1) / SEL_WARPS;
+    const int qw0 = min(nq_all, warp * nqw), qw1 = min(nq_all, qw0 + nqw);
+    const int w0 = min(i1, i0 + 4 * qw0), w1 = min(i1, i0 + 4 * qw1);
 
     // per-warp histogram of one radix digit (shared-memory atomics; lanes that hit the
     // same bin are serialised by the hardware)
@@ -206,11 +214,10 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a, 
             // four consecutive positions per thread from three 16-byte loads
             const float4* raw4 = reinterpret_cast<const float4*>(raw);
             uint4* out4 = reinterpret_cast<uint4*>(sel_dyn);                  // position i0 + 4q.. at q
-            const int nq = (i1 - i0 + 3) / 4;
-            for (int qb = 0; qb < nq; qb += SEL_THREADS) {
-                const int q = qb + tid;
+            const int nq = nq_all;
+            for (int q = qw0 + lane; q < qw1; q += 32) {
                 float o[4] = {0.f, 0.f, 0.f, 0.f};
-                if (q < nq) {
+                {
                     const float4 A = raw4[q], B = raw4[q + 1], C = raw4[q + 2];
                     const float w[12] = {A.x, A.y, A.z, A.w, B.x, B.y, B.z, B.w, C.x, C.y, C.z, C.w};
                     switch (rad) {
@@ -231,34 +238,24 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a, 
                 for (int j = 0; j < 4; ++j) hist_add(q < nq && i0 + 4 * q + j < i1, __float_as_uint(o[j]) >> 24);
             }
         } else {
-            for (int base = i0; base < i1; base += SEL_THREADS) {
-                const int i = base + tid;
-                const bool in = i < i1;
-                uint32_t v = 0u;
-                if (in) {
-                    const int t = i - i0 + pad;          // raw index of position L_sink + i
-                    float mx = raw[t - rad];
-                    for (int d = -rad + 1; d <= rad; ++d) mx = fmaxf(mx, raw[t + d]);
-                    v = __float_as_uint(mx);
-                    vals[i] = v;
-                }
-                hist_add(in, v >> 24);
+            for (int i = w0 + lane; i < w1; i += 32) {
+                const int t = i - i0 + pad;              // raw index of position L_sink + i
+                float mx = raw[t - rad];
+                for (int d = -rad + 1; d <= rad; ++d) mx = fmaxf(mx, raw[t + d]);
+                const uint32_t v = __float_as_uint(mx);
+                vals[i] = v;
+                hist_add(true, v >> 24);
             }
         }
     } else {
-        for (int base = i0; base < i1; base += SEL_THREADS) {
-            const int i = base + tid;
-            const bool in = i < i1;
-            uint32_t v = 0u;
-            if (in) {
-                const int j = c.L_sink + i;
-                const int lo = max(0, j - rad), hi = min(n_sc - 1, j + rad);
-                float mx = colsum(lo);
-                for (int k = lo + 1; k <= hi; ++k) mx = fmaxf(mx, colsum(k));
-                v = __float_as_uint(mx);
-                vals[i] = v;
-            }
-            hist_add(in, v >> 24);
+        for (int i = w0 + lane; i < w1; i += 32) {
+            const int j = c.L_sink + i;
+            const int lo = max(0, j - rad), hi = min(n_sc - 1, j + rad);
+            float mx = colsum(lo);
+            for (int k = lo + 1; k <= hi; ++k) mx = fmaxf(mx, colsum(k));
+            const uint32_t v = __float_as_uint(mx);
+            vals[i] = v;
+            hist_add(true, v >> 24);
         }
     }
     if (tid == 0) {
@@ -271,18 +268,20 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a, 
     // 1-4. radix descent over the whole middle, 8 bits at a time.  It stops early when
     //      the digit's bucket holds exactly the positions still to take: they are all
     //      kept, so the threshold becomes "at least the bucket's prefix".
+    //      Each warp also counts, from its own histogram of each pass, the positions of
+    //      its block above the final threshold (a larger digit than the pass's) and, after
+    //      the last pass, those equal to it.
     uint32_t mask = 0u;
+    int my_gt = 0, my_eq = 0;
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
         const uint32_t prefix = sh_prefix;
         if (pass > 0) {
             for (int i = lane; i < 256; i += 32) hist_w[warp][i] = 0;
             __syncwarp();
-            for (int base = i0; base < i1; base += SEL_THREADS) {
-                const int i = base + tid;
-                const bool in = i < i1;
-                const uint32_t v = in ? vals[i] : 0u;
-                hist_add(in && (v & mask) == prefix, (v >> shift) & 255u);
+            for (int i = w0 + lane; i < w1; i += 32) {
+                const uint32_t v = vals[i];
+                hist_add((v & mask) == prefix, (v >> shift) & 255u);
             }
             __syncthreads();
         }
@@ -311,6 +310,7 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a, 
             kk = __shfl_sync(0xffffffffu, kk, src);
             if (lane == 0) {
                 const uint32_t p = prefix | ((uint32_t)d << shift);
+                sh_digit = d;
                 if (pass < 3 && kk == hist_all[d] && p != 0u) {
                     // the whole bucket is kept: keep every value >= p, no ties
                     sh_prefix = p - 1u;
@@ -324,27 +324,25 @@ __global__ void __launch_bounds__(SEL_THREADS, 1) select_kernel(CompressArgs a, 
         }
         mask |= 255u << shift;
         __syncthreads();
+        {
+            // stopping early keeps the whole digit's bucket: it counts as greater
+            const int d = sh_digit;
+            const bool done = sh_done != 0;
+            int g = 0;
+            for (int b = lane; b < 256; b += 32) g += (b > d || (done && b == d)) ? hist_w[warp][b] : 0;
+            my_gt += __reduce_add_sync(0xffffffffu, g);
+            if (pass == 3 && !done) my_eq = hist_w[warp][d];
+        }
         if (sh_done) break;
     }
     const uint32_t tau = sh_prefix;
     const int kk = sh_kk;                        // how many scores equal to tau are kept
 
-    // 5. ordered compaction: warp w takes a contiguous block of the slice (whole groups
-    //    of 32 positions), its lanes reading consecutive positions; ballots order the
-    //    kept positions within each group
-    const int wrun = ((i1 - i0 + SEL_WARPS * 32 - 1) / (SEL_WARPS * 32)) * 32;
-    const int w0 = min(i1, i0 + warp * wrun), w1 = min(i1, w0 + wrun);
-    int gt = 0, eq = 0;
-    for (int i = w0 + lane; i < w1; i += 32) {
-        const uint32_t v = vals[i];
-        gt += v > tau;
-        eq += v == tau;
-    }
-    gt = __reduce_add_sync(0xffffffffu, gt);
-    eq = __reduce_add_sync(0xffffffffu, eq);
+    // 5. ordered compaction of each warp's block [w0, w1), its lanes reading consecutive
+    //    positions; ballots order the kept positions within each group of 32
     if (lane == 0) {
-        warp_gt[warp] = gt;
-        warp_eq[warp] = eq;
+        warp_gt[warp] = my_gt;
+        warp_eq[warp] = my_eq;
     }
     __syncthreads();
     if (warp == 0) {
