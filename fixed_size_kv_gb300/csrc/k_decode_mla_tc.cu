@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t dst = j < QT_CH ? s_kv + NCH * CH_B + j * QCH_B : s_q + (j - QT_CH) * QCH_B;
                 tma_load_3d(dst, &tmQ, bar(B_Q_LOAD), 64 * j, 0, b);
             }
-            constexpr int AHEAD = 4;    // tiles on their way to L2 ahead of the loads
+            constexpr int AHEAD = 2;    // tiles on their way to L2 ahead of the loads (0-2 time the same; 4: +1.4%)
             int i = 0;
             for (int t = next_tile(t_begin); t < t_end; t = next_tile(t + 1), ++i) {
                 cur_tile = t;
