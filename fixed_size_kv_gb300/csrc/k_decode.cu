@@ -33,6 +33,7 @@ constexpr int G_WARPS = 4;
 constexpr int G_STAGES = 3;
 constexpr int G_STAGE_BYTES = GQA_KEYS * G_ROWB * 2;        // K + V tile = 16 KB
 constexpr int G_SMEM = G_WARPS * G_STAGES * G_STAGE_BYTES;  // 192 KB
+static_assert(G_WARPS * 32 == GD, "the cross-warp fold gives each thread one of the GD output dimensions");
 
 __global__ void __launch_bounds__(G_WARPS * 32, 1) gqa_decode_kernel(DecodeArgs a) {
     pdl_wait();                 // the previous kernel on the stream has completed
