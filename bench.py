@@ -205,6 +205,19 @@ def algorithmic_decode_flop(wl, metas):
     return valid * wl.G * 2.0 * (wl.d_qk + wl.d_v) * wl.n_kv_heads
 
 
+def issued_decode_flop(wl, metas):
+    """FLOP the decode kernels' MMAs issue per launch.  GQA issues the algorithmic work.  The
+    MLA kernel runs two CTAs per split, each computing the whole 576-wide score of all query
+    heads and half of the value sum: per valid row 2 (2 d_qk) + 2 d_v per query head."""
+    if wl.layout == 0:
+        return algorithmic_decode_flop(wl, metas)
+    valid = 0
+    for m in metas:
+        S, T, R0, n_sink, n_mid = m
+        valid += n_sink + n_mid + min(T - R0, wl.L_recent)
+    return valid * wl.G * 2.0 * (2 * wl.d_qk + wl.d_v) * wl.n_kv_heads
+
+
 def algorithmic_decode_bytes(wl, metas):
     """Bytes one decode-attention launch must move: every valid cache row once
     (keys, plus values for GQA), the queries and the outputs."""
@@ -351,6 +364,7 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
                  [(m[0], m[1], m[2], m[3], m[4]) for m in metas]]
     attn_bytes = algorithmic_decode_bytes(wl, mid_metas)
     attn_flop = algorithmic_decode_flop(wl, mid_metas)
+    attn_issued = issued_decode_flop(wl, mid_metas)
 
     # working set of one step: prompts, cache, decode inputs and outputs
     work_bytes = sum(p.K.numel() * 2 + (p.V.numel() * 2 if p.V is not None else 0) for p in pre)
@@ -595,7 +609,11 @@ def measure(wl, args, steps, warmup, dev, stream, world, rank, full_run=True):
                      "tensor": {"flop_per_launch": attn_flop,
                                 "achieved_tflops": attn_flop / (attn_avg_ms / 1e3) / 1e12,
                                 "peak": bf16_sus,
-                                "frac": attn_flop / (attn_avg_ms / 1e3) / 1e12 / bf16_sus},
+                                "frac": attn_flop / (attn_avg_ms / 1e3) / 1e12 / bf16_sus,
+                                # on the FLOP the MMAs issue (MLA: each CTA of a pair computes
+                                # the whole score)
+                                "issued_flop_per_launch": attn_issued,
+                                "issued_frac": attn_issued / (attn_avg_ms / 1e3) / 1e12 / bf16_sus},
                      "eager_launch_ms": eager_launch_ms,
                      "timing": ("graph-replayed decode loop / steps" if graph is not None
                                 else "CUDA events around each eager launch")},

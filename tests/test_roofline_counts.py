@@ -35,6 +35,13 @@ def test_decode_bytes_and_flop_mla_128k():
     flop = bench.algorithmic_decode_flop(wl, metas)
     assert flop == 8 * 32768 * 128 * 2 * (576 + 512)
     assert abs(flop / 1e9 - 73.0) < 0.1                         # the ~73 GFLOP of one MLA step
+    # issued: each CTA of a pair computes the whole 576-wide score, and each half of P V
+    issued = bench.issued_decode_flop(wl, metas)
+    assert issued == 8 * 32768 * 128 * (2 * 2 * 576 + 2 * 512)
+    assert abs(issued / flop - (2 * 576 + 512) / (576 + 512)) < 1e-12         # 1.53x the algorithmic work
+    gqa = inputs.WORKLOADS["gqa_128k_b16"]
+    gm = [full_meta(gqa, 131072)] * 16
+    assert bench.issued_decode_flop(gqa, gm) == bench.algorithmic_decode_flop(gqa, gm)
 
 
 def test_ring_not_yet_full_counts_only_valid_rows():
